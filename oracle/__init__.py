@@ -1,0 +1,201 @@
+"""fp64 CPU oracle for Dynamic Short Convolutions (DSC) -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product library (the CUDA kernels behind
+the C ABI) never touches it, and it shares no code with them.
+
+The arithmetic lives in ``dsc_oracle.c`` (plain fp64 loops, one function per
+definition; see the comment block at its top for the passages each follows).
+This module only marshals torch CPU tensors into it and returns fp64 torch
+tensors.  Inputs may be float64, float32 or bfloat16; the C side decodes them
+exactly, so the oracle sees the values the GPU sees.
+
+Every function takes an optional ``rows`` (int64 tensor of token indices
+b*T + t); the outputs then hold only those rows, in that order.
+"""
+import ctypes
+
+import torch
+
+from .build import LIB, build_oracle
+
+_DT = {torch.float64: 0, torch.float32: 1, torch.bfloat16: 2}
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build_oracle()
+        lib = ctypes.CDLL(LIB)
+        P, I64, INT = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.orc_headwise_fwd.argtypes = [P, INT, P, INT, P, I64, I64, I64, I64,
+                                         I64, INT, P, I64]
+        lib.orc_lowrank_fwd.argtypes = [P, INT, P, INT, P, INT, P, I64, I64,
+                                        I64, I64, I64, I64, INT, P, I64]
+        lib.orc_lowrank_filters.argtypes = [P, INT, P, INT, P, I64, I64, I64,
+                                            I64, I64, I64]
+        lib.orc_headwise_bwd.argtypes = [P, INT, P, INT, P, INT, P, P, I64, I64,
+                                         I64, I64, I64, INT, P, I64]
+        lib.orc_lowrank_bwd_rows.argtypes = [P, INT, P, INT, P, INT, P, INT, P,
+                                             P, P, I64, I64, I64, I64, I64,
+                                             I64, INT, P, I64]
+        lib.orc_lowrank_dU.argtypes = [P, INT, P, INT, P, INT, P, I64, I64,
+                                       I64, I64, I64, I64]
+        for f in ("orc_headwise_fwd", "orc_lowrank_fwd", "orc_lowrank_filters",
+                  "orc_headwise_bwd", "orc_lowrank_bwd_rows", "orc_lowrank_dU"):
+            getattr(lib, f).restype = INT
+        lib.orc_num_threads.restype = INT
+        lib.orc_set_num_threads.argtypes = [INT]
+        _lib = lib
+    return _lib
+
+
+def _in(t):
+    t = t.detach()
+    if t.device.type != "cpu":
+        t = t.cpu()
+    t = t.contiguous()
+    if t.dtype not in _DT:
+        raise TypeError(f"oracle input dtype {t.dtype} not supported")
+    return t, ctypes.c_void_p(t.data_ptr()), _DT[t.dtype]
+
+
+def _rows(rows, n_all):
+    if rows is None:
+        return None, None, n_all
+    r = torch.as_tensor(rows, dtype=torch.int64).contiguous()
+    return r, ctypes.c_void_p(r.data_ptr()), r.numel()
+
+
+def _out(*shape):
+    return torch.empty(shape, dtype=torch.float64)
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise RuntimeError(f"oracle {name} failed (bad argument or out of memory)")
+
+
+def num_threads() -> int:
+    return _load().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().orc_set_num_threads(int(n))
+
+
+def headwise_fwd(x, w, H, residual, rows=None):
+    """y [B,T,C] (or [len(rows),C]) of the head-wise DSC forward."""
+    lib = _load()
+    B, T, C = x.shape
+    W = w.shape[-1]
+    xk, xp, xd = _in(x)
+    wk, wp, wd = _in(w)
+    rk, rp, n = _rows(rows, B * T)
+    y = _out(n, C)
+    _check(lib.orc_headwise_fwd(xp, xd, wp, wd, ctypes.c_void_p(y.data_ptr()),
+                                B, T, C, H, W, int(residual), rp, n), "headwise_fwd")
+    return y.view(B, T, C) if rows is None else y
+
+
+def headwise_bwd(x, w, dy, H, residual, rows=None):
+    """(dx, dw) of the head-wise DSC backward, full or for the listed rows."""
+    lib = _load()
+    B, T, C = x.shape
+    W = w.shape[-1]
+    G = C // H
+    xk, xp, xd = _in(x)
+    wk, wp, wd = _in(w)
+    gk, gp, gd = _in(dy)
+    rk, rp, n = _rows(rows, B * T)
+    dx = _out(n, C)
+    dw = _out(n, G, W)
+    _check(lib.orc_headwise_bwd(xp, xd, wp, wd, gp, gd,
+                                ctypes.c_void_p(dx.data_ptr()),
+                                ctypes.c_void_p(dw.data_ptr()),
+                                B, T, C, H, W, int(residual), rp, n), "headwise_bwd")
+    if rows is None:
+        return dx.view(B, T, C), dw.view(B, T, G, W)
+    return dx, dw
+
+
+def lowrank_filters(z, U, C, H, W):
+    """Materialised w [B,T,G,W] = z U (fp64), the naive low-rank path."""
+    lib = _load()
+    B, T, R = z.shape
+    G = C // H
+    zk, zp, zd = _in(z)
+    uk, up, ud = _in(U)
+    w = _out(B, T, G, W)
+    _check(lib.orc_lowrank_filters(zp, zd, up, ud, ctypes.c_void_p(w.data_ptr()),
+                                   B, T, C, H, W, R), "lowrank_filters")
+    return w
+
+
+def lowrank_fwd(x, z, U, H, W, residual, rows=None):
+    """y of the low-rank DSC forward (filters z_t U formed in fp64)."""
+    lib = _load()
+    B, T, C = x.shape
+    R = z.shape[-1]
+    xk, xp, xd = _in(x)
+    zk, zp, zd = _in(z)
+    uk, up, ud = _in(U)
+    rk, rp, n = _rows(rows, B * T)
+    y = _out(n, C)
+    _check(lib.orc_lowrank_fwd(xp, xd, zp, zd, up, ud,
+                               ctypes.c_void_p(y.data_ptr()), B, T, C, H, W, R,
+                               int(residual), rp, n), "lowrank_fwd")
+    return y.view(B, T, C) if rows is None else y
+
+
+def lowrank_bwd_rows(x, z, U, dy, H, W, residual, rows=None, want_dw=False):
+    """(dx, dz[, dw]) of the low-rank backward, full or for the listed rows."""
+    lib = _load()
+    B, T, C = x.shape
+    R = z.shape[-1]
+    G = C // H
+    xk, xp, xd = _in(x)
+    zk, zp, zd = _in(z)
+    uk, up, ud = _in(U)
+    gk, gp, gd = _in(dy)
+    rk, rp, n = _rows(rows, B * T)
+    dx = _out(n, C)
+    dz = _out(n, R)
+    dw = _out(n, G, W) if want_dw else None
+    _check(lib.orc_lowrank_bwd_rows(
+        xp, xd, zp, zd, up, ud, gp, gd, ctypes.c_void_p(dx.data_ptr()),
+        ctypes.c_void_p(dz.data_ptr()),
+        ctypes.c_void_p(dw.data_ptr()) if want_dw else None,
+        B, T, C, H, W, R, int(residual), rp, n), "lowrank_bwd_rows")
+    if rows is None:
+        dx, dz = dx.view(B, T, C), dz.view(B, T, R)
+        dw = dw.view(B, T, G, W) if want_dw else None
+    return (dx, dz, dw) if want_dw else (dx, dz)
+
+
+def lowrank_dU(x, z, dy, H, W):
+    """dU [R, G*W] = sum over all tokens of z_t^T dw_t, in token order."""
+    lib = _load()
+    B, T, C = x.shape
+    R = z.shape[-1]
+    G = C // H
+    xk, xp, xd = _in(x)
+    zk, zp, zd = _in(z)
+    gk, gp, gd = _in(dy)
+    dU = _out(R, G * W)
+    _check(lib.orc_lowrank_dU(xp, xd, zp, zd, gp, gd,
+                              ctypes.c_void_p(dU.data_ptr()), B, T, C, H, W, R),
+           "lowrank_dU")
+    return dU
+
+
+def lowrank_bwd(x, z, U, dy, H, W, residual):
+    """(dx, dz, dU) of the low-rank backward over the whole batch."""
+    dx, dz = lowrank_bwd_rows(x, z, U, dy, H, W, residual)
+    return dx, dz, lowrank_dU(x, z, dy, H, W)
+
+
+__all__ = ["headwise_fwd", "headwise_bwd", "lowrank_filters", "lowrank_fwd",
+           "lowrank_bwd_rows", "lowrank_dU", "lowrank_bwd", "num_threads",
+           "set_num_threads", "LIB", "build_oracle"]
