@@ -1,0 +1,460 @@
+"""Benchmark of the DSC hot path on B300.
+
+One step = the whole hot path over one batch at C=6144, W=4:
+  head-wise DSC forward + backward on the QKV placement
+      (B=8, T=2048, C=6144, H=16 -> w [8,2048,384,4], bf16, residual), and
+  low-rank fused DSC forward + backward on the same x shape
+      (R=16, H=1, U [16, 24576], bf16, residual).
+The metric is achieved HBM GB/s: the algorithmic (compulsory) bytes of the
+four calls -- every tensor read or written once, halos and partial sums
+excluded -- divided by the step time.  Inputs (0.45 GB and 0.40 GB per call)
+are larger than the 126 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dsc|reference]
+
+Under torchrun each rank runs the full workload on its own GPU (independent
+replicas; no data-path collective), the timing is max over ranks, and the
+value is the bytes of all ranks over that time.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, each
+step a bounded sample (the first 128 tokens of one sequence) of the same
+workload; it prints the same JSON line with "impl": "reference".
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from lm_local_sequence_causal_b300 import dsc, synthetic as syn  # noqa: E402
+
+METRIC = "DSC fwd+bwd achieved HBM GB/s (% of B300 peak) and Mtokens/s at C=6144, W=4"
+WORKLOAD = ("DSC at C=6144 W=4, B=8 T=2048 (16384 tokens), bf16, residual: head-wise "
+            "H=16 fwd+bwd and low-rank R=16 H=1 fwd+bwd")
+KERNEL_SOURCES = {
+    "headwise_fwd": "lm_local_sequence_causal_b300/csrc/headwise.cu",
+    "headwise_bwd": "lm_local_sequence_causal_b300/csrc/headwise.cu",
+    "lowrank_fwd": "lm_local_sequence_causal_b300/csrc/lowrank_simt.cu",
+    "lowrank_bwd": "lm_local_sequence_causal_b300/csrc/lowrank_simt.cu",
+}
+# What bounds each entry point as built: its roofline denominator.
+KERNEL_BOUND = {"headwise_fwd": "hbm", "headwise_bwd": "hbm",
+                "lowrank_fwd": "alu", "lowrank_bwd": "alu"}
+# fp32 FMA peak of the CUDA cores: 148 SMs x 128 lanes x 2 flop x 2.032 GHz.
+ALU_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+FALLBACK_HBM_GBS = 6400.0
+
+
+# ------------------------------------------------------------ byte model ----
+
+def algorithmic(wl):
+    """(fwd bytes, bwd bytes, fwd flops, bwd flops) of one call pair."""
+    s = torch.empty((), dtype=wl.dtype).element_size()
+    N, C, G, W, R = wl.tokens, wl.C, wl.G, wl.W, wl.R
+    if wl.lowrank:
+        fb = s * (2 * N * C + N * R + R * G * W)
+        bb = s * (3 * N * C + 2 * N * R + 2 * R * G * W)
+        ff = 2 * N * G * W * R + 2 * N * C * W
+        bf = 6 * N * G * W * R + 3 * N * C * W
+    else:
+        fb = s * (2 * N * C + N * G * W)
+        bb = s * (3 * N * C + 2 * N * G * W)
+        ff = 2 * N * C * W
+        bf = 4 * N * C * W
+    return fb, bb, ff, bf
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(path):
+    with open(os.path.join(ROOT, path), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def recorded_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since the counters were taken; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    e = d.get(name)
+    if not e or e.get("source_sha256_16") != source_hash(KERNEL_SOURCES[name]):
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------ clocks --------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            gid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gid],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ the step ------
+
+class Problem:
+    """Device buffers for one step of the hot path."""
+
+    def __init__(self, device, seed=0):
+        self.hw = syn.qkv_headwise()
+        self.lr = syn.qkv_lowrank()
+        self.a = syn.make_inputs(self.hw, seed, device=device)
+        self.b = syn.make_inputs(self.lr, seed + 1, device=device)
+        a, b = self.a, self.b
+        self.y_hw = torch.empty_like(a["x"])
+        self.dx_hw = torch.empty_like(a["x"])
+        self.dw_hw = torch.empty_like(a["w"])
+        self.y_lr = torch.empty_like(b["x"])
+        self.dx_lr = torch.empty_like(b["x"])
+        self.dz_lr = torch.empty_like(b["z"])
+        self.dU_lr = torch.empty_like(b["U"])
+        self.ws = dsc.lowrank_workspace(b["x"], b["z"], self.lr.H, self.lr.W)
+
+    def calls(self):
+        a, b, hw, lr = self.a, self.b, self.hw, self.lr
+        return [
+            ("headwise_fwd", lambda: dsc.dsc_headwise_fwd(a["x"], a["w"], self.y_hw, hw.H, True)),
+            ("headwise_bwd", lambda: dsc.dsc_headwise_bwd(a["x"], a["w"], a["dy"], self.dx_hw,
+                                                          self.dw_hw, hw.H, True)),
+            ("lowrank_fwd", lambda: dsc.dsc_lowrank_fwd(b["x"], b["z"], b["U"], self.y_lr,
+                                                        lr.H, lr.W, True)),
+            ("lowrank_bwd", lambda: dsc.dsc_lowrank_bwd(b["x"], b["z"], b["U"], b["dy"],
+                                                        self.dx_lr, self.dz_lr, self.dU_lr,
+                                                        self.ws, lr.H, lr.W, True)),
+        ]
+
+    LAUNCHES_PER_STEP = 5   # hw fwd, hw bwd, lr fwd, lr bwd main + lr bwd reduce
+
+    def bytes_flops(self):
+        hf, hb, hff, hbf = algorithmic(self.hw)
+        lf, lb, lff, lbf = algorithmic(self.lr)
+        return ({"headwise_fwd": hf, "headwise_bwd": hb, "lowrank_fwd": lf, "lowrank_bwd": lb},
+                {"headwise_fwd": hff, "headwise_bwd": hbf, "lowrank_fwd": lff,
+                 "lowrank_bwd": lbf})
+
+    def input_tensors(self):
+        return [self.a["x"], self.a["w"], self.a["dy"], self.b["x"], self.b["z"], self.b["U"],
+                self.b["dy"]]
+
+    def output_tensors(self):
+        return [self.y_hw, self.dx_hw, self.dw_hw, self.y_lr, self.dx_lr, self.dz_lr, self.dU_lr]
+
+
+# ------------------------------------------------------------ distributed ---
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("gloo")
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    t = torch.tensor([float(v)], dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def oracle_pass(sample_hw, sample_lr):
+    """One fp64 oracle pass of the hot path over a sample; returns seconds."""
+    import oracle as orc
+    hw, lr = sample_hw, sample_lr
+    t0 = time.perf_counter()
+    orc.headwise_fwd(hw["x"], hw["w"], 16, True)
+    orc.headwise_bwd(hw["x"], hw["w"], hw["dy"], 16, True)
+    orc.lowrank_fwd(lr["x"], lr["z"], lr["U"], 1, 4, True)
+    orc.lowrank_bwd(lr["x"], lr["z"], lr["U"], lr["dy"], 1, 4, True)
+    return time.perf_counter() - t0
+
+
+def sample_inputs(full, nseq, ntok):
+    out = {}
+    for k, v in full.items():
+        out[k] = v.cpu() if k == "U" else v[:nseq, :ntok].contiguous().cpu()
+    return out
+
+
+def sample_bytes(nseq, ntok):
+    hw = syn.qkv_headwise().with_(B=nseq, T=ntok)
+    lr = syn.qkv_lowrank().with_(B=nseq, T=ntok)
+    hf, hb, _, _ = algorithmic(hw)
+    lf, lb, _, _ = algorithmic(lr)
+    return hf + hb + lf + lb
+
+
+def cpu_baseline(prob):
+    import oracle as orc
+    nseq, ntok = 2, 2048
+    s_hw = sample_inputs(prob.a, nseq, ntok)
+    s_lr = sample_inputs(prob.b, nseq, ntok)
+    sec = oracle_pass(s_hw, s_lr)
+    gbs = sample_bytes(nseq, ntok) / sec / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"{nseq} of 8 sequences (T=2048, {nseq * ntok} tokens) of both "
+                      f"workloads, fwd+bwd, fp64, {sec:.2f} s",
+            "seconds": round(sec, 3), "mtok_per_s": round(nseq * ntok / sec / 1e6, 5)}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle as orc
+    hw = syn.qkv_headwise().with_(B=1, T=128)
+    lr = syn.qkv_lowrank().with_(B=1, T=128)
+    s_hw = syn.make_inputs(hw, 0)
+    s_lr = syn.make_inputs(lr, 1)
+    for _ in range(args.warmup):
+        oracle_pass(s_hw, s_lr)
+    tot = 0.0
+    for _ in range(args.steps):
+        tot += oracle_pass(s_hw, s_lr)
+    sec = tot / args.steps
+    nbytes = sample_bytes(1, 128)
+    gbs = nbytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(),
+        "cpu_baseline": {"kind": "oracle", "cores": orc.num_threads(),
+                         "sample": "first 128 tokens of one sequence of both workloads, "
+                                   "fwd+bwd, fp64 oracle on the host cores",
+                         "value": round(gbs, 4)},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "mtok_per_s": round(128 / sec / 1e6, 6),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict():
+    return {"workload": WORKLOAD, "B": 8, "T": 2048, "C": 6144, "W": 4,
+            "headwise_H": 16, "lowrank_R": 16, "lowrank_H": 1, "residual": True,
+            "l2": "inputs larger than L2 (0.45 GB / 0.40 GB per call), no flush",
+            "parallelism": "replicas (one full workload per GPU)"}
+
+
+# ------------------------------------------------------------ main ----------
+
+def run_dsc(args):
+    ws, rank, local = dist_env()
+    init_dist(ws)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsc.load()
+    prob = Problem(dev, seed=0)
+    calls = prob.calls()
+    nbytes, nflops = prob.bytes_flops()
+    step_bytes = sum(nbytes.values())
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        for _, f in calls:
+            f()
+    torch.cuda.synchronize()
+
+    # per-call events inside the timed region, on the launching stream
+    ev = {name: [] for name, _ in calls}
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev)
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(args.steps):
+        for name, f in calls:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            f()
+            e1.record(stream)
+            ev[name].append((e0, e1))
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_local = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms_local, ws)
+    per_call_ms = {n: sum(a.elapsed_time(b) for a, b in v) / len(v) for n, v in ev.items()}
+
+    # end to end: pinned host inputs -> device, the four calls, outputs -> host
+    e2e = run_e2e(prob, calls, args.e2e_steps) if args.e2e_steps > 0 else None
+    if e2e is not None:
+        e2e_ms = max_over_ranks(e2e["ms_per_step"], ws)
+        e2e["value"] = round(ws * step_bytes / (e2e_ms * 1e-3) / 1e9, 2)
+        e2e["ms_per_step"] = round(e2e_ms, 3)
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peaks()
+    value = ws * step_bytes / (ms * 1e-3) / 1e9
+    dom = max(per_call_ms, key=per_call_ms.get)
+    bound = KERNEL_BOUND[dom]
+    if bound == "hbm":
+        achieved = nbytes[dom] / (per_call_ms[dom] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4)}
+    else:
+        achieved = nflops[dom] / (per_call_ms[dom] * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": round(achieved, 2),
+                "peak": round(ALU_PEAK_TFLOPS, 2), "unit": "TFLOP/s",
+                "frac": round(achieved / ALU_PEAK_TFLOPS, 4)}
+    roof.update({"kernel": dom, "traffic": recorded_traffic(dom),
+                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if bound == "hbm"
+                 else "derived: 148 SMs x 128 fp32 lanes x 2 flop x 2.032 GHz"})
+    kernels = {}
+    for n in per_call_ms:
+        t = per_call_ms[n] * 1e-3
+        kernels[n] = {"ms": round(per_call_ms[n], 4), "gbs": round(nbytes[n] / t / 1e9, 1),
+                      "frac_of_hbm_peak": round(nbytes[n] / t / 1e9 / peak, 4),
+                      "tflops": round(nflops[n] / t / 1e12, 2), "bound": KERNEL_BOUND[n]}
+    N = prob.hw.tokens
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(),
+        "frac_of_hbm_peak": round(value / ws / peak, 4), "peak_gbs": peak,
+        "mtok_per_s": {
+            "headwise": round(N / ((per_call_ms["headwise_fwd"] + per_call_ms["headwise_bwd"])
+                                   * 1e-3) / 1e6, 2),
+            "lowrank": round(N / ((per_call_ms["lowrank_fwd"] + per_call_ms["lowrank_bwd"])
+                                  * 1e-3) / 1e6, 2)},
+        "kernels": kernels, "roofline": roof,
+        "gpu_launches": Problem.LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(prob)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(prob, calls, steps):
+    """The same metric through the public API with host buffers: every step
+    copies its inputs from pinned host memory and reads every output back."""
+    ins = prob.input_tensors()
+    outs = prob.output_tensors()
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    stream = torch.cuda.current_stream()
+    bi = sum(t.numel() * t.element_size() for t in ins)
+    bo = sum(t.numel() * t.element_size() for t in outs)
+
+    def step():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        for _, f in calls:
+            f()
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"value": None, "unit": "GB/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="dsc", choices=["dsc", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_dsc(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

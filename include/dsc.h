@@ -1,0 +1,142 @@
+/*
+ * dsc.h -- C ABI of the B300 (sm_103a) Dynamic Short Convolution library,
+ * libdsc.so.
+ *
+ * The operation (from "Technische Samenvatting: Dynamische Korte Convoluties
+ * Verbeteren Transformers", Methodologie: Mechanisme, Parametrisatie,
+ * Plaatsing; and "Dynamic Short Convolutions: The 'Locality Bias'
+ * Transformers Were Missing", Methodology, section 1):
+ *
+ *   y[b,t,c] = residual * x[b,t,c] + sum_{k=0}^{W-1} w[b,t,g(c),k] * x[b,t-k,c]
+ *
+ * with x[b,t-k,c] = 0 for t-k < 0 (zero padding per sequence b, no carried
+ * state), g(c) = floor(c / H) (one filter shared by H consecutive channels)
+ * and G = C / H filters per token.  In the low-rank parameterisation the
+ * filters are w[b,t,g,k] = sum_r z[b,t,r] * U[r, g*W + k]; they are formed
+ * on-chip and never written to memory (same summary, Efficiente
+ * Trainingsimplementatie: Fused Low-Rank Kernel).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every tensor argument is a pointer to DEVICE memory, dense and
+ * row-major (last index fastest), owned by the caller:
+ *     x, y, dy, dx : [B, T, C]
+ *     w, dw        : [B, T, G, W]            (tap k fastest)
+ *     z, dz        : [B, T, R]
+ *     U, dU        : [R, G*W]                (column j = g*W + k)
+ * The library never allocates, frees or synchronises.  Outputs are
+ * overwritten, never accumulated into.  Outputs may not alias inputs.
+ * Element type.  All tensors of one call share `dtype`: DSC_F32 (fp32) or
+ * DSC_BF16 (bfloat16).  Arithmetic is fp32; a bf16 result is rounded to
+ * nearest-even once, after the fp32 sum (the residual included).
+ * Ordering.  Work is enqueued on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream) and runs asynchronously; the call returns once it
+ * is enqueued.
+ * Shapes.  B >= 0, T >= 0 (B*T == 0 is a no-op), C >= 1, H >= 1, C % H == 0,
+ * 1 <= W <= 4 (W > 4 gives DSC_ERR_UNSUPPORTED).  C must be a multiple of 8
+ * (bf16) or 4 (fp32), and every pointer 16-byte aligned, else
+ * DSC_ERR_ALIGNMENT.  Any T is accepted, including T < W.
+ * Errors.  Arguments are validated on the host before anything is
+ * enqueued; a failed check returns its status and enqueues nothing.  A CUDA
+ * launch failure returns DSC_ERR_CUDA.  The library never aborts, traps or
+ * asserts.
+ */
+#ifndef DSC_H_
+#define DSC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSC_OK = 0,
+  DSC_ERR_INVALID_ARG = 1, /* null pointer, negative size, C % H != 0, ...  */
+  DSC_ERR_ALIGNMENT = 2,   /* pointer not 16-byte aligned, C not a multiple */
+  DSC_ERR_UNSUPPORTED = 3, /* valid but not built: W > 4, R > 32, ...       */
+  DSC_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required    */
+  DSC_ERR_CUDA = 5         /* a CUDA call failed (launch error)             */
+} dsc_status_t;
+
+typedef enum { DSC_F32 = 0, DSC_BF16 = 1 } dsc_dtype_t;
+
+/* Version of this ABI (bumped on any incompatible change). */
+int dsc_abi_version(void);
+
+/* Static name of a status code. */
+const char* dsc_status_string(dsc_status_t status);
+
+/*
+ * Head-wise DSC forward (Mechanisme + Parametrisatie item 2 + Plaatsing).
+ *   in : x [B,T,C], w [B,T,C/H,W]
+ *   out: y [B,T,C] = residual*x + sum_k w[.,t,g(c),k] * x[.,t-k,c]
+ * `residual` != 0 adds x (the X = X + DSC(X) placement).
+ */
+dsc_status_t dsc_headwise_fwd(const void* x, const void* w, void* y,
+                              int64_t B, int64_t T, int64_t C, int64_t H,
+                              int64_t W, int residual, dsc_dtype_t dtype,
+                              void* stream);
+
+/*
+ * Head-wise DSC backward: the chain rule of dsc_headwise_fwd (the pages
+ * state no backward formula; this one is derived from the forward).
+ *   in : x [B,T,C], w [B,T,G,W], dy [B,T,C] (gradient of the loss wrt y)
+ *   out: dx [B,T,C]:   dx[b,s,c] = residual*dy[b,s,c]
+ *                                 + sum_{k: s+k<T} w[b,s+k,g(c),k] dy[b,s+k,c]
+ *        dw [B,T,G,W]: dw[b,t,g,k] = sum_{c=gH}^{gH+H-1} dy[b,t,c] x[b,t-k,c]
+ *                                    (0 for t-k < 0)
+ */
+dsc_status_t dsc_headwise_bwd(const void* x, const void* w, const void* dy,
+                              void* dx, void* dw, int64_t B, int64_t T,
+                              int64_t C, int64_t H, int64_t W, int residual,
+                              dsc_dtype_t dtype, void* stream);
+
+/*
+ * Low-rank fused DSC forward (Parametrisatie item 1; Fused Low-Rank Kernel):
+ * the filters w[b,t,g,k] = sum_r z[b,t,r] U[r,g*W+k] are generated on-chip
+ * in fp32 (never rounded, never stored) and applied at once.
+ *   in : x [B,T,C], z [B,T,R], U [R,G*W]
+ *   out: y [B,T,C]
+ * 1 <= R <= 32.  H = 1 and power-of-two H up to 32 are built; other H give
+ * DSC_ERR_UNSUPPORTED.
+ */
+dsc_status_t dsc_lowrank_fwd(const void* x, const void* z, const void* U,
+                             void* y, int64_t B, int64_t T, int64_t C,
+                             int64_t H, int64_t W, int64_t R, int residual,
+                             dsc_dtype_t dtype, void* stream);
+
+/*
+ * Bytes of device workspace dsc_lowrank_bwd needs for these arguments
+ * (deterministic fp32 partial sums of dz and dU).  0 for an empty problem
+ * or unsupported arguments.
+ */
+size_t dsc_lowrank_bwd_workspace_size(int64_t B, int64_t T, int64_t C,
+                                      int64_t H, int64_t W, int64_t R,
+                                      dsc_dtype_t dtype);
+
+/*
+ * Low-rank fused DSC backward: the chain rule of dsc_lowrank_fwd.
+ *   in : x [B,T,C], z [B,T,R], U [R,G*W], dy [B,T,C]
+ *   out: dx [B,T,C]  (as dsc_headwise_bwd, with the generated filters)
+ *        dz [B,T,R]: dz[b,t,r] = sum_j dw[b,t,j] U[r,j]
+ *        dU [R,G*W]: dU[r,j]   = sum_{b,t} z[b,t,r] dw[b,t,j]
+ *   where dw is the head-wise filter gradient, kept on-chip in fp32.
+ * workspace: caller-owned device memory of at least
+ * dsc_lowrank_bwd_workspace_size(...) bytes, 16-byte aligned; its contents
+ * on entry do not matter and are clobbered.  Partial sums are combined in a
+ * fixed order, so results are bitwise reproducible run to run.
+ */
+dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U,
+                             const void* dy, void* dx, void* dz, void* dU,
+                             void* workspace, size_t workspace_bytes,
+                             int64_t B, int64_t T, int64_t C, int64_t H,
+                             int64_t W, int64_t R, int residual,
+                             dsc_dtype_t dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSC_H_ */

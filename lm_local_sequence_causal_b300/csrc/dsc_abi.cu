@@ -1,0 +1,138 @@
+// dsc_abi.cu -- the extern "C" entry points declared in include/dsc.h:
+// host-side validation, then dispatch to the kernel files.  Nothing here
+// allocates, frees or synchronises.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsc.h"
+#include "dsc_internal.h"
+
+namespace {
+
+using dsc::Shape;
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Shape checks common to every entry point.  `R` is 0 for head-wise.
+dsc_status_t check_shape(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
+                         int64_t R, dsc_dtype_t dt, bool lowrank) {
+  if (dt != DSC_F32 && dt != DSC_BF16) return DSC_ERR_INVALID_ARG;
+  if (B < 0 || T < 0 || C < 1 || H < 1 || W < 1) return DSC_ERR_INVALID_ARG;
+  if (C % H != 0) return DSC_ERR_INVALID_ARG;
+  if (lowrank && R < 1) return DSC_ERR_INVALID_ARG;
+  // Index arithmetic is 64-bit; keep the element counts far from overflow.
+  if (B > (int64_t(1) << 31) || T > (int64_t(1) << 31) || C > (int64_t(1) << 24))
+    return DSC_ERR_INVALID_ARG;
+  if (W > 4) return DSC_ERR_UNSUPPORTED;
+  const int64_t vec = dt == DSC_BF16 ? 8 : 4;
+  if (C % vec != 0) return DSC_ERR_ALIGNMENT;
+  return DSC_OK;
+}
+
+dsc_status_t check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr) return DSC_ERR_INVALID_ARG;
+  for (const void* p : ps)
+    if (!aligned16(p)) return DSC_ERR_ALIGNMENT;
+  return DSC_OK;
+}
+
+Shape make_shape(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W, int64_t R,
+                 int residual, dsc_dtype_t dt) {
+  return Shape{B, T, C, H, W, R, residual ? 1 : 0, dt == DSC_BF16 ? 1 : 0};
+}
+
+dsc_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSC_OK : DSC_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int dsc_abi_version(void) { return 1; }
+
+const char* dsc_status_string(dsc_status_t s) {
+  switch (s) {
+    case DSC_OK: return "DSC_OK";
+    case DSC_ERR_INVALID_ARG: return "DSC_ERR_INVALID_ARG";
+    case DSC_ERR_ALIGNMENT: return "DSC_ERR_ALIGNMENT";
+    case DSC_ERR_UNSUPPORTED: return "DSC_ERR_UNSUPPORTED";
+    case DSC_ERR_WORKSPACE: return "DSC_ERR_WORKSPACE";
+    case DSC_ERR_CUDA: return "DSC_ERR_CUDA";
+  }
+  return "DSC_ERR_UNKNOWN";
+}
+
+dsc_status_t dsc_headwise_fwd(const void* x, const void* w, void* y, int64_t B, int64_t T,
+                              int64_t C, int64_t H, int64_t W, int residual,
+                              dsc_dtype_t dtype, void* stream) {
+  dsc_status_t st = check_shape(B, T, C, H, W, 0, dtype, false);
+  if (st != DSC_OK) return st;
+  if (B * T == 0) return DSC_OK;
+  if ((st = check_ptrs({x, w, y})) != DSC_OK) return st;
+  if (x == y) return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::headwise_fwd(x, w, y, make_shape(B, T, C, H, W, 0, residual, dtype),
+                                     (cudaStream_t)stream));
+}
+
+dsc_status_t dsc_headwise_bwd(const void* x, const void* w, const void* dy, void* dx,
+                              void* dw, int64_t B, int64_t T, int64_t C, int64_t H,
+                              int64_t W, int residual, dsc_dtype_t dtype, void* stream) {
+  dsc_status_t st = check_shape(B, T, C, H, W, 0, dtype, false);
+  if (st != DSC_OK) return st;
+  if (B * T == 0) return DSC_OK;
+  if ((st = check_ptrs({x, w, dy, dx, dw})) != DSC_OK) return st;
+  if (dx == x || dx == dy || dx == dw || dw == x || dw == w || dw == dy)
+    return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::headwise_bwd(x, w, dy, dx, dw,
+                                     make_shape(B, T, C, H, W, 0, residual, dtype),
+                                     (cudaStream_t)stream));
+}
+
+dsc_status_t dsc_lowrank_fwd(const void* x, const void* z, const void* U, void* y,
+                             int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
+                             int64_t R, int residual, dsc_dtype_t dtype, void* stream) {
+  dsc_status_t st = check_shape(B, T, C, H, W, R, dtype, true);
+  if (st != DSC_OK) return st;
+  const Shape s = make_shape(B, T, C, H, W, R, residual, dtype);
+  if (!dsc::lowrank_supported(s)) return DSC_ERR_UNSUPPORTED;
+  if (B * T == 0) return DSC_OK;
+  if ((st = check_ptrs({x, z, U, y})) != DSC_OK) return st;
+  if (x == y) return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::lowrank_fwd(x, z, U, y, s, (cudaStream_t)stream));
+}
+
+size_t dsc_lowrank_bwd_workspace_size(int64_t B, int64_t T, int64_t C, int64_t H,
+                                      int64_t W, int64_t R, dsc_dtype_t dtype) {
+  if (check_shape(B, T, C, H, W, R, dtype, true) != DSC_OK) return 0;
+  const Shape s = make_shape(B, T, C, H, W, R, 0, dtype);
+  if (!dsc::lowrank_supported(s) || B * T == 0) return 0;
+  return dsc::lowrank_bwd_workspace(s);
+}
+
+dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U, const void* dy,
+                             void* dx, void* dz, void* dU, void* workspace,
+                             size_t workspace_bytes, int64_t B, int64_t T, int64_t C,
+                             int64_t H, int64_t W, int64_t R, int residual,
+                             dsc_dtype_t dtype, void* stream) {
+  dsc_status_t st = check_shape(B, T, C, H, W, R, dtype, true);
+  if (st != DSC_OK) return st;
+  const Shape s = make_shape(B, T, C, H, W, R, residual, dtype);
+  if (!dsc::lowrank_supported(s)) return DSC_ERR_UNSUPPORTED;
+  if (B * T == 0) {
+    // dU is a sum over zero tokens: all zeros.  Nothing else to write.
+    if (dU == nullptr) return DSC_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)R * (C / H) * W * (dtype == DSC_BF16 ? 2 : 4);
+    return from_cuda(cudaMemsetAsync(dU, 0, bytes, (cudaStream_t)stream));
+  }
+  if ((st = check_ptrs({x, z, U, dy, dx, dz, dU})) != DSC_OK) return st;
+  if (dx == x || dx == dy || dz == z || dU == U) return DSC_ERR_INVALID_ARG;
+  const size_t need = dsc::lowrank_bwd_workspace(s);
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need) return DSC_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DSC_ERR_ALIGNMENT;
+  }
+  return from_cuda(dsc::lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, s,
+                                    (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,193 @@
+"""Thin ctypes binding to libdsc.so (the C ABI of include/dsc.h).
+
+The functions named like the C entry points (``dsc_headwise_fwd`` ...) take
+torch CUDA tensors for the pointer arguments and only marshal them: check
+dtype, contiguity and device, pass ``data_ptr()`` and the current CUDA
+stream, and raise ``DSCError`` on any status other than DSC_OK.  All the
+arithmetic runs in the CUDA kernels; there is no CPU or PyTorch fallback.
+If the library is missing the first call raises.
+
+``headwise_fwd`` and friends are conveniences that allocate the outputs
+with torch and call the entry points.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsc.so")
+
+DSC_OK, DSC_ERR_INVALID_ARG, DSC_ERR_ALIGNMENT = 0, 1, 2
+DSC_ERR_UNSUPPORTED, DSC_ERR_WORKSPACE, DSC_ERR_CUDA = 3, 4, 5
+DSC_F32, DSC_BF16 = 0, 1
+_DTYPES = {torch.float32: DSC_F32, torch.bfloat16: DSC_BF16}
+
+_lib = None
+
+
+class DSCError(RuntimeError):
+    def __init__(self, status, name):
+        self.status = status
+        super().__init__(f"{name} failed: {status_string(status)} ({status})")
+
+
+def load():
+    """Load libdsc.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libdsc.so not found at {LIB_PATH}; build it with "
+                           "`python -m lm_local_sequence_causal_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, INT, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.dsc_abi_version.restype = INT
+    lib.dsc_status_string.argtypes = [INT]
+    lib.dsc_status_string.restype = ctypes.c_char_p
+    lib.dsc_headwise_fwd.argtypes = [P, P, P, I64, I64, I64, I64, I64, INT, INT, P]
+    lib.dsc_headwise_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, INT, INT, P]
+    lib.dsc_lowrank_fwd.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, I64, INT, INT, P]
+    lib.dsc_lowrank_bwd_workspace_size.argtypes = [I64, I64, I64, I64, I64, I64, INT]
+    lib.dsc_lowrank_bwd_workspace_size.restype = SZ
+    lib.dsc_lowrank_bwd.argtypes = [P, P, P, P, P, P, P, P, SZ, I64, I64, I64, I64, I64,
+                                    I64, INT, INT, P]
+    for f in ("dsc_headwise_fwd", "dsc_headwise_bwd", "dsc_lowrank_fwd", "dsc_lowrank_bwd"):
+        getattr(lib, f).restype = INT
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().dsc_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return load().dsc_abi_version()
+
+
+# ------------------------------------------------------------ marshalling ----
+
+def _ptr(t, dtype, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t):
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+    return _DTYPES[t.dtype]
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc, name):
+    if rc != DSC_OK:
+        raise DSCError(rc, name)
+
+
+def _bt_c(x):
+    if x.dim() != 3:
+        raise ValueError("x must be [B, T, C]")
+    return x.shape
+
+
+# --------------------------------------------------- the C entry points ------
+
+def dsc_headwise_fwd(x, w, y, H, residual=True, stream=None):
+    """y[b,t,c] = residual*x + sum_k w[b,t,c//H,k] x[b,t-k,c]   (in place into y)."""
+    B, T, C = _bt_c(x)
+    W = w.shape[-1]
+    dt = x.dtype
+    _check(load().dsc_headwise_fwd(_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(y, dt, "y"),
+                                   B, T, C, H, W, int(bool(residual)), _dtype_code(x),
+                                   _stream(stream)), "dsc_headwise_fwd")
+
+
+def dsc_headwise_bwd(x, w, dy, dx, dw, H, residual=True, stream=None):
+    """dx, dw of the head-wise DSC (written in place)."""
+    B, T, C = _bt_c(x)
+    W = w.shape[-1]
+    dt = x.dtype
+    _check(load().dsc_headwise_bwd(_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(dy, dt, "dy"),
+                                   _ptr(dx, dt, "dx"), _ptr(dw, dt, "dw"), B, T, C, H, W,
+                                   int(bool(residual)), _dtype_code(x), _stream(stream)),
+           "dsc_headwise_bwd")
+
+
+def dsc_lowrank_fwd(x, z, U, y, H, W, residual=True, stream=None):
+    """y of the low-rank fused DSC (filters z_t U formed on-chip)."""
+    B, T, C = _bt_c(x)
+    R = z.shape[-1]
+    dt = x.dtype
+    _check(load().dsc_lowrank_fwd(_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"),
+                                  _ptr(y, dt, "y"), B, T, C, H, W, R, int(bool(residual)),
+                                  _dtype_code(x), _stream(stream)), "dsc_lowrank_fwd")
+
+
+def dsc_lowrank_bwd_workspace_size(B, T, C, H, W, R, dtype) -> int:
+    return int(load().dsc_lowrank_bwd_workspace_size(B, T, C, H, W, R, _DTYPES[dtype]))
+
+
+def dsc_lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, H, W, residual=True, stream=None):
+    """dx, dz, dU of the low-rank fused DSC; `workspace` is a uint8 CUDA tensor."""
+    B, T, C = _bt_c(x)
+    R = z.shape[-1]
+    dt = x.dtype
+    ws_ptr = _ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(load().dsc_lowrank_bwd(_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"),
+                                  _ptr(dy, dt, "dy"), _ptr(dx, dt, "dx"), _ptr(dz, dt, "dz"),
+                                  _ptr(dU, dt, "dU"), ws_ptr, ws_bytes, B, T, C, H, W, R,
+                                  int(bool(residual)), _dtype_code(x), _stream(stream)),
+           "dsc_lowrank_bwd")
+
+
+# ------------------------------------------------------- conveniences --------
+
+def headwise_fwd(x, w, H, residual=True):
+    y = torch.empty_like(x)
+    dsc_headwise_fwd(x, w, y, H, residual)
+    return y
+
+
+def headwise_bwd(x, w, dy, H, residual=True):
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(w)
+    dsc_headwise_bwd(x, w, dy, dx, dw, H, residual)
+    return dx, dw
+
+
+def lowrank_fwd(x, z, U, H, W, residual=True):
+    y = torch.empty_like(x)
+    dsc_lowrank_fwd(x, z, U, y, H, W, residual)
+    return y
+
+
+def lowrank_workspace(x, z, H, W):
+    B, T, C = x.shape
+    n = dsc_lowrank_bwd_workspace_size(B, T, C, H, W, z.shape[-1], x.dtype)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=x.device)
+
+
+def lowrank_bwd(x, z, U, dy, H, W, residual=True, workspace=None):
+    dx = torch.empty_like(x)
+    dz = torch.empty_like(z)
+    dU = torch.empty_like(U)
+    if workspace is None:
+        workspace = lowrank_workspace(x, z, H, W)
+    dsc_lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, H, W, residual)
+    return dx, dz, dU

@@ -1,0 +1,119 @@
+"""The C ABI on the CPU: libdsc.so loads, exports every entry point that
+include/dsc.h declares, and rejects bad arguments on the host before any
+CUDA call (no GPU is touched: every case below returns during validation;
+the non-null pointers are never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from lm_local_sequence_causal_b300 import dsc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsc.h")
+
+P = ctypes.c_void_p
+A = P(0x10000)          # 16-byte aligned stand-in address (never dereferenced)
+A2 = P(0x20000)
+A3 = P(0x30000)
+A4 = P(0x40000)
+A5 = P(0x50000)
+MIS = P(0x10002)        # misaligned stand-in address
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsc_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return dsc.load()
+
+
+def test_header_declares_the_four_kernels_and_helpers():
+    names = declared_functions()
+    for n in ("dsc_headwise_fwd", "dsc_headwise_bwd", "dsc_lowrank_fwd", "dsc_lowrank_bwd",
+              "dsc_lowrank_bwd_workspace_size", "dsc_status_string", "dsc_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libdsc.so does not export {name}"
+
+
+def test_status_strings(lib):
+    assert dsc.status_string(dsc.DSC_OK) == "DSC_OK"
+    assert dsc.status_string(dsc.DSC_ERR_WORKSPACE) == "DSC_ERR_WORKSPACE"
+    assert dsc.abi_version() == 1
+
+
+BF16, F32 = dsc.DSC_BF16, dsc.DSC_F32
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (x, w, y, B, T, C, H, W, residual, dtype)
+    ((A, A2, A3, 2, 8, 64, 1, 0, 1, BF16), dsc.DSC_ERR_INVALID_ARG),   # W = 0
+    ((A, A2, A3, 2, 8, 64, 1, 5, 1, BF16), dsc.DSC_ERR_UNSUPPORTED),   # W > 4
+    ((A, A2, A3, 2, 8, 64, 3, 4, 1, BF16), dsc.DSC_ERR_INVALID_ARG),   # C % H != 0
+    ((A, A2, A3, 2, 8, 12, 1, 4, 1, BF16), dsc.DSC_ERR_ALIGNMENT),     # C % 8 != 0 (bf16)
+    ((None, None, None, 0, 8, 12, 1, 4, 1, F32), dsc.DSC_OK),          # C % 4 == 0 is enough for fp32
+    ((A, A2, A3, -1, 8, 64, 1, 4, 1, BF16), dsc.DSC_ERR_INVALID_ARG),  # B < 0
+    ((None, A2, A3, 2, 8, 64, 1, 4, 1, BF16), dsc.DSC_ERR_INVALID_ARG),  # null x
+    ((MIS, A2, A3, 2, 8, 64, 1, 4, 1, BF16), dsc.DSC_ERR_ALIGNMENT),   # misaligned x
+    ((A, A, A, 2, 8, 64, 1, 4, 1, BF16), dsc.DSC_ERR_INVALID_ARG),     # y aliases x
+    ((A, A2, A3, 2, 8, 64, 1, 4, 1, 7), dsc.DSC_ERR_INVALID_ARG),      # bad dtype
+    ((None, None, None, 0, 8, 64, 1, 4, 1, BF16), dsc.DSC_OK),         # empty: no-op
+    ((None, None, None, 3, 0, 64, 1, 4, 1, BF16), dsc.DSC_OK),         # empty: no-op
+])
+def test_headwise_fwd_validation(lib, args, expect):
+    x, w, y, B, T, C, H, W, res, dt = args
+    rc = lib.dsc_headwise_fwd(x, w, y, B, T, C, H, W, res, dt, None)
+    assert rc == expect, dsc.status_string(rc)
+
+
+def test_headwise_bwd_validation(lib):
+    f = lib.dsc_headwise_bwd
+    assert f(A, A2, A3, A4, A5, 2, 8, 64, 1, 9, 1, BF16, None) == dsc.DSC_ERR_UNSUPPORTED
+    assert f(A, A2, A3, None, A5, 2, 8, 64, 1, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, A4, MIS, 2, 8, 64, 1, 4, 1, BF16, None) == dsc.DSC_ERR_ALIGNMENT
+    assert f(A, A2, A3, A, A5, 2, 8, 64, 1, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, A4, A4, 2, 8, 64, 1, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(None, None, None, None, None, 0, 5, 64, 1, 4, 1, F32, None) == dsc.DSC_OK
+
+
+def test_lowrank_validation_and_workspace(lib):
+    f = lib.dsc_lowrank_fwd
+    # R out of range / H not built
+    assert f(A, A2, A3, A4, 2, 8, 64, 1, 4, 0, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, A4, 2, 8, 64, 1, 4, 33, 1, BF16, None) == dsc.DSC_ERR_UNSUPPORTED
+    assert f(A, A2, A3, A4, 2, 8, 96, 3, 4, 16, 1, BF16, None) == dsc.DSC_ERR_UNSUPPORTED
+    assert f(A, MIS, A3, A4, 2, 8, 64, 1, 4, 16, 1, BF16, None) == dsc.DSC_ERR_ALIGNMENT
+    ws = lib.dsc_lowrank_bwd_workspace_size
+    n = ws(8, 2048, 6144, 1, 4, 16, BF16)
+    assert n > 0 and n % 256 == 0
+    assert ws(8, 2048, 6144, 1, 4, 40, BF16) == 0      # unsupported R
+    assert ws(0, 2048, 6144, 1, 4, 16, BF16) == 0      # empty
+    g = lib.dsc_lowrank_bwd
+    # workspace missing or too small: rejected before launch
+    assert g(A, A2, A3, A4, A5, P(0x60000), P(0x70000), None, 0,
+             8, 2048, 6144, 1, 4, 16, 1, BF16, None) == dsc.DSC_ERR_WORKSPACE
+    assert g(A, A2, A3, A4, A5, P(0x60000), P(0x70000), P(0x80000), n - 16,
+             8, 2048, 6144, 1, 4, 16, 1, BF16, None) == dsc.DSC_ERR_WORKSPACE
+    assert g(A, A2, A3, A4, A5, P(0x60000), P(0x70000), P(0x80008), n,
+             8, 2048, 6144, 1, 4, 16, 1, BF16, None) == dsc.DSC_ERR_ALIGNMENT
+    # dx aliasing x
+    assert g(A, A2, A3, A4, A, P(0x60000), P(0x70000), P(0x80000), n,
+             8, 2048, 6144, 1, 4, 16, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 4, 8)
+    w = torch.zeros(1, 4, 8, 4)
+    with pytest.raises(ValueError):
+        dsc.headwise_fwd(x, w, 1)
