@@ -135,6 +135,41 @@ dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U,
                              int64_t W, int64_t R, int residual,
                              dsc_dtype_t dtype, void* stream);
 
+/*
+ * Largest workspace dsc_lowrank_bwd_noalloc can provide: 32 MiB.
+ */
+#define DSC_LOWRANK_BWD_NOALLOC_MAX_BYTES ((size_t)32 << 20)
+
+/*
+ * dsc_lowrank_bwd for callers that cannot allocate device memory.  The
+ * paper has no counterpart to this entry point; it exists for library
+ * users.  Some callers cannot call cudaMalloc: a plugin inside a host
+ * program that owns all device memory, a service with a fixed memory budget
+ * that forbids allocation after start-up, or a latency-critical path that
+ * cannot afford the device synchronisation an allocation may cause.  This
+ * variant takes no workspace argument; it uses a fixed 32 MiB array compiled
+ * into the library (every GPU that loads the library holds it until the
+ * process exits) and calls no allocating routine.
+ *   Arguments, layouts, results and errors are those of dsc_lowrank_bwd.
+ *   A problem whose workspace (dsc_lowrank_bwd_workspace_size) exceeds
+ *   DSC_LOWRANK_BWD_NOALLOC_MAX_BYTES is refused with DSC_ERR_WORKSPACE
+ *   before anything is enqueued; use dsc_lowrank_bwd for it.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.  The stream must belong to the current device.
+ *   All calls share the one array: two calls whose work overlaps on the GPU
+ *   (different streams, or different host threads, without ordering between
+ *   them) race on it and give wrong results.  Calls ordered on one stream
+ *   are safe; nothing needs clearing between them, since every partial sum
+ *   is written before it is read.
+ */
+dsc_status_t dsc_lowrank_bwd_noalloc(const void* x, const void* z,
+                                     const void* U, const void* dy, void* dx,
+                                     void* dz, void* dU, int64_t B, int64_t T,
+                                     int64_t C, int64_t H, int64_t W,
+                                     int64_t R, int residual,
+                                     dsc_dtype_t dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
