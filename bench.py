@@ -43,12 +43,12 @@ WORKLOAD = ("DSC at C=6144 W=4, B=8 T=2048 (16384 tokens), bf16, residual: head-
 KERNEL_SOURCES = {
     "headwise_fwd": "lm_local_sequence_causal_b300/csrc/headwise.cu",
     "headwise_bwd": "lm_local_sequence_causal_b300/csrc/headwise.cu",
-    "lowrank_fwd": "lm_local_sequence_causal_b300/csrc/lowrank_simt.cu",
+    "lowrank_fwd": "lm_local_sequence_causal_b300/csrc/lowrank_tc.cu",
     "lowrank_bwd": "lm_local_sequence_causal_b300/csrc/lowrank_simt.cu",
 }
 # What bounds each entry point as built: its roofline denominator.
 KERNEL_BOUND = {"headwise_fwd": "hbm", "headwise_bwd": "hbm",
-                "lowrank_fwd": "alu", "lowrank_bwd": "alu"}
+                "lowrank_fwd": "hbm", "lowrank_bwd": "alu"}
 # fp32 FMA peak of the CUDA cores: 148 SMs x 128 lanes x 2 flop x 2.032 GHz.
 ALU_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 FALLBACK_HBM_GBS = 6400.0

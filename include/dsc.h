@@ -136,6 +136,25 @@ dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U,
                              dsc_dtype_t dtype, void* stream);
 
 /*
+ * 1 if dsc_lowrank_fwd / dsc_lowrank_bwd run these arguments on the tensor
+ * cores (tcgen05: bf16, H = 1, R = 16 or 32, 1 <= W <= 4), 0 if they run the
+ * CUDA-core kernels, -1 if the arguments are invalid or unsupported.  Host
+ * only; touches no device.
+ */
+int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H,
+                                  int64_t W, int64_t R, dsc_dtype_t dtype);
+
+/*
+ * Diagnostic: the device error word of the tensor-core kernels on the
+ * current device.  0 means no error; otherwise it holds the code of the
+ * first bounded wait that gave up (1 producer, 2 MMA issuer, 3 epilogue,
+ * 4 store), after which that kernel returned early and its outputs are
+ * invalid.  `reset` != 0 clears the word.  Synchronous (it copies one word
+ * from the device); not meant for the hot path.
+ */
+dsc_status_t dsc_device_error(unsigned int* code, int reset);
+
+/*
  * Largest workspace dsc_lowrank_bwd_noalloc can provide: 32 MiB.
  */
 #define DSC_LOWRANK_BWD_NOALLOC_MAX_BYTES ((size_t)32 << 20)

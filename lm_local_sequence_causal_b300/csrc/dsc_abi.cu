@@ -98,6 +98,10 @@ dsc_status_t dsc_lowrank_fwd(const void* x, const void* z, const void* U, void* 
   if (B * T == 0) return DSC_OK;
   if ((st = check_ptrs({x, z, U, y})) != DSC_OK) return st;
   if (x == y) return DSC_ERR_INVALID_ARG;
+  if (dsc::lowrank_tc_supported(s)) {
+    const cudaError_t e = dsc::lowrank_fwd_tc(x, z, U, y, s, (cudaStream_t)stream);
+    if (e != cudaErrorNotSupported) return from_cuda(e);
+  }
   return from_cuda(dsc::lowrank_fwd(x, z, U, y, s, (cudaStream_t)stream));
 }
 
@@ -133,6 +137,19 @@ dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U, const 
   }
   return from_cuda(dsc::lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, s,
                                     (cudaStream_t)stream));
+}
+
+int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
+                                  int64_t R, dsc_dtype_t dtype) {
+  if (check_shape(B, T, C, H, W, R, dtype, true) != DSC_OK) return -1;
+  const Shape s = make_shape(B, T, C, H, W, R, 0, dtype);
+  if (!dsc::lowrank_supported(s)) return -1;
+  return dsc::lowrank_tc_supported(s) ? 1 : 0;
+}
+
+dsc_status_t dsc_device_error(unsigned int* code, int reset) {
+  if (code == nullptr) return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::lowrank_tc_error(code, reset != 0));
 }
 
 }  // extern "C"

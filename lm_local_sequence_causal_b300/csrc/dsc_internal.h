@@ -2,6 +2,7 @@
 // and the kernel files.  Arguments here are already validated.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -30,5 +31,22 @@ size_t lowrank_bwd_workspace(const Shape& s);
 cudaError_t lowrank_bwd(const void* x, const void* z, const void* U,
                         const void* dy, void* dx, void* dz, void* dU,
                         void* ws, const Shape& s, cudaStream_t st);
+
+// Tensor-core (tcgen05) low-rank kernels (lowrank_tc.cu): bf16, H = 1,
+// R in {16, 32}.  The *_tc functions return cudaErrorNotSupported when the
+// shape is outside that set, so the caller can use the CUDA-core kernels.
+bool lowrank_tc_supported(const Shape& s);
+cudaError_t lowrank_fwd_tc(const void* x, const void* z, const void* U, void* y,
+                           const Shape& s, cudaStream_t st);
+// Device error word of the tensor-core kernels (0 = no error; otherwise the
+// code of the bounded wait that gave up).  Synchronous; diagnostic only.
+cudaError_t lowrank_tc_error(unsigned int* out, bool reset);
+
+// Host helpers (tmap.cu).
+// 3-D tensor map over a dense row-major [d2][d1][d0] tensor of bf16 or fp32,
+// box {b0, b1, 1}, swizzle 0/32/64/128 bytes, zero fill out of range.
+bool make_tmap_3d(CUtensorMap* tm, const void* base, bool bf16, uint64_t d0, uint64_t d1,
+                  uint64_t d2, uint32_t b0, uint32_t b1, int swizzle_bytes);
+int sm_count();
 
 }  // namespace dsc

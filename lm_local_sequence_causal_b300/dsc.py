@@ -52,6 +52,10 @@ def load():
     lib.dsc_lowrank_bwd_workspace_size.restype = SZ
     lib.dsc_lowrank_bwd.argtypes = [P, P, P, P, P, P, P, P, SZ, I64, I64, I64, I64, I64,
                                     I64, INT, INT, P]
+    lib.dsc_lowrank_uses_tensor_cores.argtypes = [I64, I64, I64, I64, I64, I64, INT]
+    lib.dsc_lowrank_uses_tensor_cores.restype = INT
+    lib.dsc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), INT]
+    lib.dsc_device_error.restype = INT
     for f in ("dsc_headwise_fwd", "dsc_headwise_bwd", "dsc_lowrank_fwd", "dsc_lowrank_bwd"):
         getattr(lib, f).restype = INT
     _lib = lib
@@ -64,6 +68,18 @@ def status_string(status: int) -> str:
 
 def abi_version() -> int:
     return load().dsc_abi_version()
+
+
+def dsc_lowrank_uses_tensor_cores(B, T, C, H, W, R, dtype) -> int:
+    """1: tensor-core kernels, 0: CUDA-core kernels, -1: invalid/unsupported."""
+    return int(load().dsc_lowrank_uses_tensor_cores(B, T, C, H, W, R, _DTYPES[dtype]))
+
+
+def dsc_device_error(reset=False) -> int:
+    """Error word of the tensor-core kernels on the current device (0 = none)."""
+    code = ctypes.c_uint(0)
+    _check(load().dsc_device_error(ctypes.byref(code), int(bool(reset))), "dsc_device_error")
+    return int(code.value)
 
 
 # ------------------------------------------------------------ marshalling ----

@@ -117,3 +117,22 @@ def test_binding_rejects_cpu_tensors():
     w = torch.zeros(1, 4, 8, 4)
     with pytest.raises(ValueError):
         dsc.headwise_fwd(x, w, 1)
+
+
+def test_lowrank_path_query():
+    q = dsc.dsc_lowrank_uses_tensor_cores
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    # the headline low-rank workload and the sweep / linear-RNN shapes run on tcgen05
+    assert q(8, 2048, 6144, 1, 4, 16, bf) == 1
+    assert q(32, 512, 5632, 1, 3, 16, bf) == 1
+    assert q(2, 16384, 4096, 1, 4, 16, bf) == 1
+    assert q(2, 100, 256, 1, 2, 32, bf) == 1
+    # everything else takes the CUDA-core kernels
+    assert q(8, 2048, 6144, 1, 4, 16, f32) == 0        # fp32 keeps exact fp32 filters
+    assert q(8, 2048, 6144, 4, 4, 16, bf) == 0         # tied filters (H > 1)
+    assert q(8, 2048, 6144, 1, 4, 8, bf) == 0
+    # invalid or unbuilt arguments
+    assert q(8, 2048, 6144, 1, 4, 0, bf) == -1
+    assert q(8, 2048, 6144, 1, 5, 16, bf) == -1
+    assert q(8, 2048, 6144, 3, 4, 16, bf) == -1
