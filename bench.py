@@ -44,11 +44,11 @@ KERNEL_SOURCES = {
     "headwise_fwd": "lm_local_sequence_causal_b300/csrc/headwise.cu",
     "headwise_bwd": "lm_local_sequence_causal_b300/csrc/headwise.cu",
     "lowrank_fwd": "lm_local_sequence_causal_b300/csrc/lowrank_tc.cu",
-    "lowrank_bwd": "lm_local_sequence_causal_b300/csrc/lowrank_simt.cu",
+    "lowrank_bwd": "lm_local_sequence_causal_b300/csrc/lowrank_tc.cu",
 }
 # What bounds each entry point as built: its roofline denominator.
 KERNEL_BOUND = {"headwise_fwd": "hbm", "headwise_bwd": "hbm",
-                "lowrank_fwd": "hbm", "lowrank_bwd": "alu"}
+                "lowrank_fwd": "hbm", "lowrank_bwd": "hbm"}
 # fp32 FMA peak of the CUDA cores: 148 SMs x 128 lanes x 2 flop x 2.032 GHz.
 ALU_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 FALLBACK_HBM_GBS = 6400.0
@@ -182,7 +182,8 @@ class Problem:
                                                         self.ws, lr.H, lr.W, True)),
         ]
 
-    LAUNCHES_PER_STEP = 5   # hw fwd, hw bwd, lr fwd, lr bwd main + lr bwd reduce
+    # hw fwd, hw bwd, lr fwd, lr bwd (U image, main kernel, partial-sum reduction)
+    LAUNCHES_PER_STEP = 6
 
     def bytes_flops(self):
         hf, hb, hff, hbf = algorithmic(self.hw)

@@ -136,10 +136,11 @@ dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U,
                              dsc_dtype_t dtype, void* stream);
 
 /*
- * 1 if dsc_lowrank_fwd / dsc_lowrank_bwd run these arguments on the tensor
- * cores (tcgen05: bf16, H = 1, R = 16 or 32, 1 <= W <= 4), 0 if they run the
- * CUDA-core kernels, -1 if the arguments are invalid or unsupported.  Host
- * only; touches no device.
+ * Which low-rank kernels these arguments run on: bit 0 set if
+ * dsc_lowrank_fwd uses the tensor cores (tcgen05: bf16, H = 1, R = 16 or
+ * 32, 1 <= W <= 4), bit 1 set if dsc_lowrank_bwd does (bf16, H = 1,
+ * R = 16, 1 <= W <= 4); a clear bit means the CUDA-core kernels.  -1 if the
+ * arguments are invalid or unsupported.  Host only; touches no device.
  */
 int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H,
                                   int64_t W, int64_t R, dsc_dtype_t dtype);

@@ -110,6 +110,7 @@ size_t dsc_lowrank_bwd_workspace_size(int64_t B, int64_t T, int64_t C, int64_t H
   if (check_shape(B, T, C, H, W, R, dtype, true) != DSC_OK) return 0;
   const Shape s = make_shape(B, T, C, H, W, R, 0, dtype);
   if (!dsc::lowrank_supported(s) || B * T == 0) return 0;
+  if (dsc::lowrank_bwd_tc_supported(s)) return dsc::lowrank_bwd_tc_workspace(s);
   return dsc::lowrank_bwd_workspace(s);
 }
 
@@ -130,11 +131,15 @@ dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U, const 
   }
   if ((st = check_ptrs({x, z, U, dy, dx, dz, dU})) != DSC_OK) return st;
   if (dx == x || dx == dy || dz == z || dU == U) return DSC_ERR_INVALID_ARG;
-  const size_t need = dsc::lowrank_bwd_workspace(s);
+  const bool tc = dsc::lowrank_bwd_tc_supported(s);
+  const size_t need = tc ? dsc::lowrank_bwd_tc_workspace(s) : dsc::lowrank_bwd_workspace(s);
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need) return DSC_ERR_WORKSPACE;
     if (!aligned16(workspace)) return DSC_ERR_ALIGNMENT;
   }
+  if (tc)
+    return from_cuda(dsc::lowrank_bwd_tc(x, z, U, dy, dx, dz, dU, workspace, s,
+                                         (cudaStream_t)stream));
   return from_cuda(dsc::lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, s,
                                     (cudaStream_t)stream));
 }
@@ -144,7 +149,7 @@ int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H, in
   if (check_shape(B, T, C, H, W, R, dtype, true) != DSC_OK) return -1;
   const Shape s = make_shape(B, T, C, H, W, R, 0, dtype);
   if (!dsc::lowrank_supported(s)) return -1;
-  return dsc::lowrank_tc_supported(s) ? 1 : 0;
+  return (dsc::lowrank_tc_supported(s) ? 1 : 0) | (dsc::lowrank_bwd_tc_supported(s) ? 2 : 0);
 }
 
 dsc_status_t dsc_device_error(unsigned int* code, int reset) {

@@ -38,6 +38,12 @@ cudaError_t lowrank_bwd(const void* x, const void* z, const void* U,
 bool lowrank_tc_supported(const Shape& s);
 cudaError_t lowrank_fwd_tc(const void* x, const void* z, const void* U, void* y,
                            const Shape& s, cudaStream_t st);
+// Backward on the tensor cores: bf16, H = 1, R = 16 (a subset of the above).
+bool lowrank_bwd_tc_supported(const Shape& s);
+size_t lowrank_bwd_tc_workspace(const Shape& s);
+cudaError_t lowrank_bwd_tc(const void* x, const void* z, const void* U, const void* dy,
+                           void* dx, void* dz, void* dU, void* ws, const Shape& s,
+                           cudaStream_t st);
 // Device error word of the tensor-core kernels (0 = no error; otherwise the
 // code of the bounded wait that gave up).  Synchronous; diagnostic only.
 cudaError_t lowrank_tc_error(unsigned int* out, bool reset);
@@ -47,6 +53,9 @@ cudaError_t lowrank_tc_error(unsigned int* out, bool reset);
 // box {b0, b1, 1}, swizzle 0/32/64/128 bytes, zero fill out of range.
 bool make_tmap_3d(CUtensorMap* tm, const void* base, bool bf16, uint64_t d0, uint64_t d1,
                   uint64_t d2, uint32_t b0, uint32_t b1, int swizzle_bytes);
+// 4-D bf16 tensor map with explicit strides (bytes) of dims 1..3, no swizzle.
+bool make_tmap_4d_bf16(CUtensorMap* tm, const void* base, const uint64_t dims[4],
+                       const uint64_t strides_bytes[3], const uint32_t box[4]);
 int sm_count();
 
 }  // namespace dsc

@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "dsc_common.cuh"
@@ -311,6 +312,508 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   }
 }
 
+// ------------------------------------------------------------ backward ----
+//
+// Chain rule of the forward (the pages state no backward; this is derived):
+//   dx[s,c]   = res*dy[s,c] + sum_{k: s+k<T} w[s+k,c,k] dy[s+k,c]
+//   dw[t,c,k] = dy[t,c] x[t-k,c]                          (kept on-chip, bf16)
+//   dz[t,r]   = sum_{c,k} dw[t,c,k] U[r,c*W+k]            (over all channels)
+//   dU[r,c*W+k] = sum_{b,t} z[t,r] dw[t,c,k]              (over all tokens)
+// One pass over x, dy, z per (128-token tile, 64-channel chunk) item, four
+// kinds of tensor-core MMA (all M = 128, fp32 accumulators in TMEM):
+//   D_k[s,c]  = sum_r z[s+k,r] U[r,c*W+k]   (N = 64, K = R; the z operand is a
+//               row-interleaved tile whose start moves 16 bytes per row, so
+//               the shift by k tokens is a descriptor offset)  -> dx
+//   dz[t,r]  += dw[t,:] U[r,:]^T            (N = R, K = 64*W; dw K-major)
+//   dU^T[j,r]+= dw[:,j]^T z[:,r]            (N = R, K = 128 tokens; dw read
+//               MN-major from the same tile, z MN-major from the same tile
+//               as the D_k operand)
+// dw lives in four 16 KB tiles (one per tap, 128 tokens x 64 channels,
+// 128-byte swizzle), written once by the epilogue and read by both
+// contractions.  The grid is S channel slices x P token splits; a CTA walks
+// its slice chunk by chunk and, inside a chunk, its split tile by tile.  It
+// keeps the dz accumulators of all its tiles and the dU accumulator of its
+// current chunk in TMEM, and writes one fp32 partial per (slice, token) and
+// per (split, column); a second kernel adds them in a fixed order.
+//
+// Roles: warp 0 producer (TMA boxes of x [t0-W+1, t0+128), dy [t0, t0+127+W)
+// and z [t0, t0+127+W), plus one 1-D bulk copy of the chunk's U tiles per
+// chunk), warp 1 TMEM owner and MMA issuer, warps 2-9 epilogue.  Per item
+// the epilogue (a) reads D_k and dy, writes dx (staged, TMA store) and frees
+// D so the MMA of the next item can start, (b) forms dw into the dw tiles;
+// at chunk ends it reads out the dU accumulator, at the end the dz ones.
+
+template <int W>
+struct BwdLayout {
+  static constexpr int NT = W <= 2 ? 2 : 4;               // dw taps incl. zero padding
+  static constexpr int XROWS = BM + W - 1;
+  static constexpr int XBOX = XROWS * 128;
+  static constexpr int XBYTES = round1k(XBOX);
+  static constexpr int ZBOX = XROWS * 32;                 // [2 halves][XROWS][16 B]
+  static constexpr int ZBYTES = round1k(ZBOX);
+  static constexpr int NSTB = 3;
+  static constexpr int STAGE = 2 * XBYTES + ZBYTES;       // x, dy, z
+  static constexpr int UBYTES = W * 2048;                 // U tiles of one chunk
+  static constexpr int UALLOC = round1k(UBYTES);
+  static constexpr int DWTAP = BM * 128;                  // one tap of dw (16 KB)
+  static constexpr int STG_OFF = 0;
+  static constexpr int U_OFF = NSTB * STAGE;
+  static constexpr int DW_OFF = U_OFF + 2 * UALLOC;
+  static constexpr int DX_OFF = DW_OFF + NT * DWTAP;
+  static constexpr int BAR_OFF = DX_OFF + BM * 128;
+  // full[3] empty[3] dfull dempty dwfull dwfree ufull[2] ufree[2] uafull[2]
+  // uaempty[2] dzfull yfull yfree
+  static constexpr int NBAR = 2 * NSTB + 4 + 8 + 3;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int TOTAL = MISC_OFF + 16 + 1024;
+  static constexpr uint32_t TX = 2 * XBOX + ZBOX;
+  static constexpr int TM_D = 0;                          // W x 64 columns
+  static constexpr int TM_DU = W * 64;                    // 2 buffers x NT/2 x 16
+  static constexpr int TM_DZ = TM_DU + NT * 16;           // 16 per tile of the split
+  static constexpr int TPS_MAX = (512 - TM_DZ) / 16;
+};
+
+// Shared-memory descriptors of the layouts above (fields as in sm100.cuh).
+// layout: 0 = no swizzle (8-row x 16-byte core matrices), 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(layout) << 61);
+}
+
+// kind::f16 instruction descriptor with operand majors (0 = K-major, 1 = MN-major).
+__host__ __device__ constexpr uint32_t idesc_major(uint32_t M, uint32_t N, uint32_t amaj,
+                                                   uint32_t bmaj) {
+  return idesc_bf16_f32(M, N) | (amaj << 15) | (bmaj << 16);
+}
+
+struct BwdArgs {
+  float* dz_part;          // [S][B*T][16]
+  float* dU_part;          // [P][16][C*W]
+  const unsigned char* uimg;  // [nchunks][W][16 rows][128 B] swizzled U tiles
+  int T, C, ntiles, nchunks, S, P, ntl, residual;
+};
+
+template <int W>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+          const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dx,
+          const BwdArgs args) {
+  using L = BwdLayout<W>;
+  constexpr int NST_ = L::NSTB;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = align1k(smem_raw);
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // This CTA's channel slice [ch0, ch1) and token-tile split [tl0, tl1).
+  const int slice = blockIdx.x % args.S, split = blockIdx.x / args.S;
+  const int ch0 = static_cast<int>(static_cast<long long>(args.nchunks) * slice / args.S);
+  const int ch1 = static_cast<int>(static_cast<long long>(args.nchunks) * (slice + 1) / args.S);
+  const int tl0 = static_cast<int>(static_cast<long long>(args.ntl) * split / args.P);
+  const int tl1 = static_cast<int>(static_cast<long long>(args.ntl) * (split + 1) / args.P);
+  const int ntile = tl1 - tl0, nchunk = ch1 - ch0;
+  const int nitems = ntile * nchunk;
+  const int64_t CW = static_cast<int64_t>(args.C) * W;
+  const int64_t Ntok = static_cast<int64_t>(args.ntl / args.ntiles) * args.T;
+
+  const uint32_t bar_full = sb + L::BAR_OFF;
+  const uint32_t bar_empty = bar_full + NST_ * 8;
+  const uint32_t bar_dfull = bar_empty + NST_ * 8;
+  const uint32_t bar_dempty = bar_dfull + 8;
+  const uint32_t bar_dwfull = bar_dempty + 8;
+  const uint32_t bar_dwfree = bar_dwfull + 8;
+  const uint32_t bar_ufull = bar_dwfree + 8;
+  const uint32_t bar_ufree = bar_ufull + 16;
+  const uint32_t bar_uafull = bar_ufree + 16;
+  const uint32_t bar_uaempty = bar_uafull + 16;
+  const uint32_t bar_dzfull = bar_uaempty + 16;
+  const uint32_t bar_yfull = bar_dzfull + 8;
+  const uint32_t bar_yfree = bar_yfull + 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST_; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1 + NEPI);
+    }
+    mbar_init(bar_dfull, 1);
+    mbar_init(bar_dempty, NEPI);
+    mbar_init(bar_dwfull, NEPI);
+    mbar_init(bar_dwfree, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_ufull + 8 * a, 1);
+      mbar_init(bar_ufree + 8 * a, 1);
+      mbar_init(bar_uafull + 8 * a, 1);
+      mbar_init(bar_uaempty + 8 * a, NEPI);
+    }
+    mbar_init(bar_dzfull, 1);
+    mbar_init(bar_yfull, NEPI);
+    mbar_init(bar_yfree, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_dy);
+    tma_prefetch_desc(&tm_z);
+    tma_prefetch_desc(&tm_dx);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  // Taps past W of the padded dw tiles stay zero for the whole kernel.
+  for (int i = threadIdx.x; i < (L::NT - W) * L::DWTAP / 16; i += blockDim.x)
+    sts128(sb + L::DW_OFF + W * L::DWTAP + 16 * i, make_uint4(0, 0, 0, 0));
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // item n -> (local chunk lc = n / ntile, local tile lt = n % ntile)
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer --
+    if (lane == 0) {
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      int n = 0;
+      for (; n < nitems; ++n) {
+        const int lc = n / ntile, lt = n - lc * ntile;
+        if (lt == 0) {
+          const int ub = lc & 1;
+          if (!mbar_wait(bar_ufree + 8 * ub, ((lc >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 1))
+            break;
+          const uint32_t uf = bar_ufull + 8 * ub;
+          mbar_expect_tx(uf, L::UBYTES);
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+              "[%0], [%1], %2, [%3], %4;" ::"r"(sb + L::U_OFF + ub * L::UALLOC),
+              "l"(args.uimg + static_cast<size_t>(ch0 + lc) * L::UBYTES), "r"(L::UBYTES),
+              "r"(uf), "l"(pol_keep)
+              : "memory");
+        }
+        const int s = n % NST_;
+        const uint32_t ph = (n / NST_) & 1;
+        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_tc_error, 1)) break;
+        const int gt = tl0 + lt;
+        const int b = gt / args.ntiles, t0 = (gt - b * args.ntiles) * BM;
+        const int c0 = (ch0 + lc) * CC;
+        const uint32_t full = bar_full + 8 * s;
+        const uint32_t st = sb + L::STG_OFF + s * L::STAGE;
+        mbar_expect_tx(full, L::TX);
+        tma_load_3d(st, &tm_x, full, c0, t0 - (W - 1), b, pol_stream);
+        tma_load_3d(st + L::XBYTES, &tm_dy, full, c0, t0, b, pol_stream);
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+            "cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(st + 2 * L::XBYTES),
+            "l"(reinterpret_cast<uint64_t>(&tm_z)), "r"(0), "r"(t0), "r"(0), "r"(b), "r"(full),
+            "l"(pol_keep)
+            : "memory");
+      }
+      for (int j = std::max(0, n - NST_); j < n; ++j)
+        drain_wait(bar_full + 8 * (j % NST_), (j / NST_) & 1);
+      const int nl = n > 0 ? (n - 1) / ntile + 1 : 0;      // chunks whose U load was issued
+      for (int lc = std::max(0, nl - 2); lc < nl; ++lc)
+        drain_wait(bar_ufull + 8 * (lc & 1), (lc >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t id_d = idesc_major(BM, 64, 0, 1);    // A z K-major, B U MN-major
+      constexpr uint32_t id_dz = idesc_major(BM, 16, 0, 0);   // A dw K-major, B U K-major
+      constexpr uint32_t id_du = idesc_major(BM, 16, 1, 1);   // A dw^T MN-major, B z MN-major
+      const uint32_t zsbo = L::XROWS * 16;                    // stride of the two z halves
+      bool ok = true;
+      int issued_d = 0, issued_dzdu = 0;
+      for (int n = 0; n <= nitems && ok; ++n) {
+        if (n < nitems) {
+          // ---- D_k for item n
+          const int lc = n / ntile, lt = n - lc * ntile;
+          const int s = n % NST_;
+          if (lt == 0)
+            ok = ok && mbar_wait(bar_ufull + 8 * (lc & 1), (lc >> 1) & 1, abort_flag,
+                                 &g_tc_error, 2);
+          ok = ok && mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 2);
+          ok = ok && mbar_wait(bar_dempty, (n & 1) ^ 1, abort_flag, &g_tc_error, 2);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
+          const uint32_t ut = sb + L::U_OFF + (lc & 1) * L::UALLOC;
+#pragma unroll
+          for (int k = 0; k < W; ++k)
+            mma_bf16(tmem + L::TM_D + k * 64, make_desc(zt + 16 * k, zsbo, 128, 0),
+                     make_desc(ut + k * 2048, 16, 1024, 2), id_d, 0u);
+          mma_commit(bar_dfull);
+          ++issued_d;
+        }
+        if (n > 0) {
+          // ---- dz and dU for item m = n - 1
+          const int m = n - 1;
+          const int lc = m / ntile, lt = m - lc * ntile;
+          const int s = m % NST_;
+          const int ub = lc & 1;
+          ok = ok && mbar_wait(bar_dwfull, m & 1, abort_flag, &g_tc_error, 2);
+          if (lt == 0 && lc >= 2)
+            ok = ok && mbar_wait(bar_uaempty + 8 * ub, ((lc >> 1) & 1) ^ 1, abort_flag,
+                                 &g_tc_error, 2);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t dw = sb + L::DW_OFF;
+          const uint32_t ut = sb + L::U_OFF + ub * L::UALLOC;
+          const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
+          // dz[t, :] (+)= sum over the chunk's 64*W columns (tap-major)
+#pragma unroll
+          for (int q = 0; q < 4 * W; ++q) {
+            const int k = q >> 2, cb = q & 3;
+            mma_bf16(tmem + L::TM_DZ + lt * 16,
+                     make_desc(dw + k * L::DWTAP + cb * 32, 16, 1024, 2),
+                     make_desc(ut + k * 2048 + cb * 32, 16, 1024, 2), id_dz,
+                     (lc > 0 || q > 0) ? 1u : 0u);
+          }
+          // dU^T[j', :] (+)= over the tile's 128 tokens; M block mb = taps 2mb, 2mb+1
+#pragma unroll
+          for (int mb = 0; mb < L::NT / 2; ++mb)
+#pragma unroll
+            for (int ks = 0; ks < BM / 16; ++ks)
+              mma_bf16(tmem + L::TM_DU + ub * (L::NT / 2) * 16 + mb * 16,
+                       make_desc(dw + 2 * mb * L::DWTAP + ks * 2048, L::DWTAP, 1024, 2),
+                       make_desc(zt + ks * 256, 128, zsbo, 0), id_du,
+                       (lt > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar_dwfree);
+          mma_commit(bar_empty + 8 * s);
+          if (lt == ntile - 1) {
+            mma_commit(bar_uafull + 8 * ub);
+            mma_commit(bar_ufree + 8 * ub);
+          }
+          ++issued_dzdu;
+        }
+      }
+      if (ok && nitems > 0) mma_commit(bar_dzfull);
+      // Let every MMA this thread issued finish before TMEM is freed.
+      if (issued_dzdu > 0) drain_wait(bar_dwfree, (issued_dzdu - 1) & 1);
+      if (issued_d > 0) drain_wait(bar_dfull, (issued_d - 1) & 1);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue --
+    const int lg = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int tl = lg * 32 + lane;
+    const bool storer = (warp == 2 && lane == 0);
+    const uint64_t pol_y = policy_evict_first();
+    const uint32_t tlane = static_cast<uint32_t>(lg * 32) << 16;
+    const uint32_t dxs = sb + L::DX_OFF;
+    bool ok = true;
+    for (int n = 0; n < nitems; ++n) {
+      const int lc = n / ntile, lt = n - lc * ntile;
+      const int s = n % NST_;
+      const int gt = tl0 + lt;
+      const int b = gt / args.ntiles, t0 = (gt - b * args.ntiles) * BM;
+      const int c0 = (ch0 + lc) * CC;
+      const uint32_t st = sb + L::STG_OFF + s * L::STAGE;
+      const uint32_t xt = st, dyt = st + L::XBYTES;
+      if (storer) {
+        bulk_wait_read<0>();
+        mbar_arrive(bar_yfree);
+      }
+      ok = mbar_wait(bar_yfree, n & 1, abort_flag, &g_tc_error, 3) &&
+           mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3) &&
+           mbar_wait(bar_dfull, n & 1, abort_flag, &g_tc_error, 3);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      // (a) dx from D_k and dy; keep dy[t] for (b)
+      uint4 dyk[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cch = 4 * h + q;
+        uint32_t dk[W][8];
+#pragma unroll
+        for (int k = 0; k < W; ++k) tmem_ld8(tmem + tlane + L::TM_D + k * 64 + 32 * h + 8 * q, dk[k]);
+        float g[W][8];
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const uint4 raw = lds128(dyt + sw128_offset(tl + k, cch));
+          if (k == 0) dyk[q] = raw;
+          unpack16<__nv_bfloat16>(raw, g[k]);
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < W; ++k) tmem_regs_ready<8>(dk[k]);
+        float out[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float v = args.residual ? g[0][c] : 0.f;
+#pragma unroll
+          for (int k = 0; k < W; ++k) v = fmaf(__uint_as_float(dk[k][c]), g[k][c], v);
+          out[c] = v;
+        }
+        sts128(dxs + sw128_offset(tl, cch), pack16<__nv_bfloat16>(out));
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_dempty);
+        mbar_arrive(bar_yfull);
+      }
+      if (storer && mbar_wait(bar_yfull, n & 1, abort_flag, &g_tc_error, 4)) {
+        tma_store_3d(&tm_dx, dxs, c0, t0, b, pol_y);
+        bulk_commit();
+      }
+      // (b) dw[t,c,k] = dy[t,c] x[t-k,c] into the tap tiles
+      ok = mbar_wait(bar_dwfree, (n & 1) ^ 1, abort_flag, &g_tc_error, 3);
+      if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cch = 4 * h + q;
+        float g[8];
+        unpack16<__nv_bfloat16>(dyk[q], g);
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          float xv[8], p[8];
+          unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch)), xv);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) p[c] = g[c] * xv[c];
+          sts128(sb + L::DW_OFF + k * L::DWTAP + sw128_offset(tl, cch),
+                 pack16<__nv_bfloat16>(p));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_dwfull);
+        mbar_arrive(bar_empty + 8 * s);
+      }
+      // (c) end of a chunk: read out its dU^T accumulator
+      if (lt == ntile - 1) {
+        const int ub = lc & 1;
+        ok = mbar_wait(bar_uafull + 8 * ub, (lc >> 1) & 1, abort_flag, &g_tc_error, 3);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        if (h < L::NT / 2) {
+          uint32_t v[16];
+          tmem_ld16(tmem + tlane + L::TM_DU + ub * (L::NT / 2) * 16 + h * 16, v);
+          tmem_wait_ld();
+          tmem_regs_ready<16>(v);
+          const int jp = h * 128 + tl;                    // tap-major column of the chunk
+          const int k = jp >> 6, c = c0 + (jp & 63);
+          if (k < W && c < args.C) {
+            float* dst = args.dU_part + static_cast<size_t>(split) * 16 * CW +
+                         static_cast<int64_t>(c) * W + k;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) dst[static_cast<int64_t>(r) * CW] = __uint_as_float(v[r]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_uaempty + 8 * ub);
+      }
+    }
+    // (d) the dz accumulators of every tile of the split
+    if (ok && nitems > 0) {
+      ok = mbar_wait(bar_dzfull, 0, abort_flag, &g_tc_error, 3);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        for (int lt = h; lt < ntile; lt += 2) {
+          uint32_t v[16];
+          tmem_ld16(tmem + tlane + L::TM_DZ + lt * 16, v);
+          tmem_wait_ld();
+          tmem_regs_ready<16>(v);
+          const int gt = tl0 + lt;
+          const int b = gt / args.ntiles, t = (gt - b * args.ntiles) * BM + tl;
+          if (t < args.T) {
+            float4* dst = reinterpret_cast<float4*>(
+                args.dz_part + (static_cast<size_t>(slice) * Ntok +
+                                static_cast<int64_t>(b) * args.T + t) * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
+        }
+      }
+    }
+    if (storer) bulk_wait<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// U rearranged into the shared-memory image of the backward's U tiles: for
+// chunk ch and tap k, a [16 r][64 c] tile with 128-byte rows and the TMA
+// 128-byte swizzle, element (r, c) = U[r, (64*ch + c)*W + k] (zero past C).
+template <int W>
+__global__ void lr_u_image(const __nv_bfloat16* __restrict__ U, unsigned char* __restrict__ img,
+                           int C, int nchunks) {
+  const int64_t CW = static_cast<int64_t>(C) * W;
+  const int total = nchunks * W * 16 * 8;              // 16-byte pieces
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int piece = i & 7, r = (i >> 3) & 15, tile = i >> 7;
+    const int k = tile % W, ch = tile / W;
+    uint32_t w4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t pair = 0;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int c = ch * CC + piece * 8 + 2 * e + hh;
+        uint32_t bits = 0;
+        if (c < C) bits = __bfloat16_as_ushort(U[static_cast<int64_t>(r) * CW + static_cast<int64_t>(c) * W + k]);
+        pair |= bits << (16 * hh);
+      }
+      w4[e] = pair;
+    }
+    const uint32_t off = static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(piece) ^ (r & 7u)) << 4);
+    *reinterpret_cast<uint4*>(img + static_cast<size_t>(tile) * 2048 + off) =
+        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+}
+
+// dz[n, r] = sum_s dz_part[s][n][r]; dU[r, j] = sum_p dU_part[p][r][j]; fixed
+// order, fp32, rounded once to bf16.  Four outputs per thread.
+__global__ void lr_reduce_tc(const float* __restrict__ dz_part, const float* __restrict__ dU_part,
+                             __nv_bfloat16* __restrict__ dz, __nv_bfloat16* __restrict__ dU,
+                             int64_t nz4, int S, int64_t nU4, int P) {
+  const int64_t total = nz4 + nU4;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4* src;
+    int64_t stride;
+    int cnt;
+    __nv_bfloat16* out;
+    int64_t j;
+    if (i < nz4) {
+      src = reinterpret_cast<const float4*>(dz_part) + i;
+      stride = nz4;
+      cnt = S;
+      out = dz;
+      j = i;
+    } else {
+      j = i - nz4;
+      src = reinterpret_cast<const float4*>(dU_part) + j;
+      stride = nU4;
+      cnt = P;
+      out = dU;
+    }
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < cnt; ++p) {
+      const float4 v = __ldcs(src + p * stride);
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    *reinterpret_cast<uint2*>(out + 4 * j) = pk;
+  }
+}
+
 // ------------------------------------------------------------------ host ----
 
 // Opt in to large dynamic shared memory, once per kernel and device.  The
@@ -341,7 +844,7 @@ cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, con
   if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, BM + W - 1, 128) ||
       !make_tmap_3d(&tz, z, true, s.R, s.T, s.B, 16, BM, 32) ||
       !make_tmap_3d(&ty, y, true, s.C, s.T, s.B, CC, BM, 128))
-    return cudaErrorNotSupported;
+    return cudaErrorInvalidValue;
   const int ntiles = static_cast<int>((s.T + BM - 1) / BM);
   const int nchunks = static_cast<int>((s.C + CC - 1) / CC);
   const long long nbt = static_cast<long long>(s.B) * ntiles;
@@ -359,7 +862,134 @@ cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, con
   return cudaGetLastError();
 }
 
+// ---- backward host side
+
+struct TcBwdPlan {
+  int S = 0, P = 0, ntiles = 0, nchunks = 0, ntl = 0;
+  size_t dz_off = 0, dU_off = 0, img_off = 0, total = 0;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int tps_max(int64_t W) {
+  switch (W) {
+    case 1: return BwdLayout<1>::TPS_MAX;
+    case 2: return BwdLayout<2>::TPS_MAX;
+    case 3: return BwdLayout<3>::TPS_MAX;
+    default: return BwdLayout<4>::TPS_MAX;
+  }
+}
+
+// Choose S channel slices x P token splits (S * P CTAs, one per SM when
+// possible): each CTA's dz accumulators must fit TMEM (tiles per split <=
+// tps_max), and the estimate balances the largest CTA's streamed bytes
+// against the fp32 partial sums written and re-read by the reduction.
+TcBwdPlan plan_bwd_tc(const Shape& s, int nsm) {
+  TcBwdPlan p;
+  p.ntiles = static_cast<int>((s.T + BM - 1) / BM);
+  p.nchunks = static_cast<int>((s.C + CC - 1) / CC);
+  p.ntl = static_cast<int>(s.B * p.ntiles);
+  const int tmax = tps_max(s.W);
+  const double item = 3.0 * BM * CC * 2;
+  const double N = static_cast<double>(s.B) * s.T, CW = static_cast<double>(s.C) * s.W;
+  double best = -1;
+  const int pmin = (p.ntl + tmax - 1) / tmax;
+  for (int P = pmin; P <= std::max(pmin, std::min(p.ntl, nsm)); ++P) {
+    const int tps = (p.ntl + P - 1) / P;
+    if (tps > tmax) continue;
+    const int S = std::max(1, std::min(p.nchunks, nsm / P));
+    const int cps = (p.nchunks + S - 1) / S;
+    const double waves = std::ceil(static_cast<double>(S) * P / nsm);
+    const double cost = waves * cps * tps * item + 2.0 * 64.0 * (S * N + P * CW) / (S * P);
+    if (best < 0 || cost < best) {
+      best = cost;
+      p.S = S;
+      p.P = P;
+    }
+  }
+  p.dz_off = 0;
+  p.dU_off = align_up(static_cast<size_t>(p.S) * s.B * s.T * 16 * sizeof(float), 256);
+  p.img_off = p.dU_off + align_up(static_cast<size_t>(p.P) * 16 * s.C * s.W * sizeof(float), 256);
+  p.total = p.img_off + align_up(static_cast<size_t>(p.nchunks) * s.W * 2048, 256);
+  return p;
+}
+
+template <int W>
+cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* dy, void* dx,
+                       void* dz, void* dU, void* ws, const Shape& s, const TcBwdPlan& p,
+                       cudaStream_t st) {
+  using L = BwdLayout<W>;
+  CUtensorMap tx, tdy, tz, tdx;
+  const uint64_t zd[4] = {8, static_cast<uint64_t>(s.T), 2, static_cast<uint64_t>(s.B)};
+  const uint64_t zs[3] = {16 * 2, 16, static_cast<uint64_t>(s.T) * 16 * 2};
+  const uint32_t zb[4] = {8, static_cast<uint32_t>(L::XROWS), 2, 1};
+  if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
+      !make_tmap_3d(&tdy, dy, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
+      !make_tmap_3d(&tdx, dx, true, s.C, s.T, s.B, CC, BM, 128) ||
+      !make_tmap_4d_bf16(&tz, z, zd, zs, zb))
+    return cudaErrorInvalidValue;
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  BwdArgs a;
+  a.dz_part = reinterpret_cast<float*>(base + p.dz_off);
+  a.dU_part = reinterpret_cast<float*>(base + p.dU_off);
+  a.uimg = base + p.img_off;
+  a.T = static_cast<int>(s.T);
+  a.C = static_cast<int>(s.C);
+  a.ntiles = p.ntiles;
+  a.nchunks = p.nchunks;
+  a.S = p.S;
+  a.P = p.P;
+  a.ntl = p.ntl;
+  a.residual = s.residual;
+  {
+    const int pieces = p.nchunks * W * 128;
+    lr_u_image<W><<<std::min(1184, (pieces + 255) / 256), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(U), base + p.img_off, static_cast<int>(s.C),
+        p.nchunks);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = lr_bwd_tc<W>;
+  cudaError_t e = set_smem<L>(kern, L::TOTAL);
+  if (e != cudaSuccess) return e;
+  kern<<<static_cast<unsigned>(p.S * p.P), kFwdThreads, L::TOTAL, st>>>(tx, tdy, tz, tdx, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t nz4 = s.B * s.T * 16 / 4, nU4 = 16 * s.C * s.W / 4;
+  const int blocks = static_cast<int>(std::min<int64_t>((nz4 + nU4 + 255) / 256, 148 * 8));
+  lr_reduce_tc<<<blocks, 256, 0, st>>>(a.dz_part, a.dU_part, static_cast<__nv_bfloat16*>(dz),
+                                       static_cast<__nv_bfloat16*>(dU), nz4, p.S, nU4, p.P);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+bool lowrank_bwd_tc_supported(const Shape& s) {
+  return s.bf16 && s.H == 1 && s.R == 16 && s.W >= 1 && s.W <= 4 &&
+         s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.T < (int64_t(1) << 30) &&
+         s.C < (int64_t(1) << 24);
+}
+
+size_t lowrank_bwd_tc_workspace(const Shape& s) {
+  if (!lowrank_bwd_tc_supported(s)) return 0;
+  const int nsm = sm_count();
+  return plan_bwd_tc(s, nsm > 0 ? nsm : 148).total;
+}
+
+cudaError_t lowrank_bwd_tc(const void* x, const void* z, const void* U, const void* dy,
+                           void* dx, void* dz, void* dU, void* ws, const Shape& s,
+                           cudaStream_t st) {
+  if (!lowrank_bwd_tc_supported(s)) return cudaErrorNotSupported;
+  const int nsm = sm_count();
+  if (nsm <= 0) return cudaErrorNoDevice;
+  const TcBwdPlan p = plan_bwd_tc(s, nsm);
+  switch (s.W) {
+    case 1: return launch_bwd<1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+    case 2: return launch_bwd<2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+    case 3: return launch_bwd<3>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+    default: return launch_bwd<4>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+  }
+}
 
 bool lowrank_tc_supported(const Shape& s) {
   return s.bf16 && s.H == 1 && (s.R == 16 || s.R == 32) && s.W >= 1 && s.W <= 4 &&

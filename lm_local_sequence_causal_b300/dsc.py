@@ -71,7 +71,7 @@ def abi_version() -> int:
 
 
 def dsc_lowrank_uses_tensor_cores(B, T, C, H, W, R, dtype) -> int:
-    """1: tensor-core kernels, 0: CUDA-core kernels, -1: invalid/unsupported."""
+    """Bit 0: forward on the tensor cores, bit 1: backward; -1: invalid/unsupported."""
     return int(load().dsc_lowrank_uses_tensor_cores(B, T, C, H, W, R, _DTYPES[dtype]))
 
 

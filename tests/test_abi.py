@@ -123,11 +123,12 @@ def test_lowrank_path_query():
     q = dsc.dsc_lowrank_uses_tensor_cores
     import torch
     bf, f32 = torch.bfloat16, torch.float32
-    # the headline low-rank workload and the sweep / linear-RNN shapes run on tcgen05
-    assert q(8, 2048, 6144, 1, 4, 16, bf) == 1
-    assert q(32, 512, 5632, 1, 3, 16, bf) == 1
-    assert q(2, 16384, 4096, 1, 4, 16, bf) == 1
-    assert q(2, 100, 256, 1, 2, 32, bf) == 1
+    # the headline low-rank workload and the sweep / linear-RNN shapes run on
+    # tcgen05 forward (bit 0) and backward (bit 1)
+    assert q(8, 2048, 6144, 1, 4, 16, bf) == 3
+    assert q(32, 512, 5632, 1, 3, 16, bf) == 3
+    assert q(2, 16384, 4096, 1, 4, 16, bf) == 3
+    assert q(2, 100, 256, 1, 2, 32, bf) == 1          # R = 32: forward only
     # everything else takes the CUDA-core kernels
     assert q(8, 2048, 6144, 1, 4, 16, f32) == 0        # fp32 keeps exact fp32 filters
     assert q(8, 2048, 6144, 4, 4, 16, bf) == 0         # tied filters (H > 1)

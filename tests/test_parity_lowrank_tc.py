@@ -25,7 +25,7 @@ def no_device_error():
 
 
 def run_fwd(wl, seed):
-    assert dsc.dsc_lowrank_uses_tensor_cores(wl.B, wl.T, wl.C, wl.H, wl.W, wl.R, wl.dtype) == 1
+    assert dsc.dsc_lowrank_uses_tensor_cores(wl.B, wl.T, wl.C, wl.H, wl.W, wl.R, wl.dtype) & 1
     inp = syn.make_inputs(wl, seed, device="cuda")
     y = Guarded(inp["x"].shape, wl.dtype)
     dsc.dsc_lowrank_fwd(inp["x"], inp["z"], inp["U"], y.t, wl.H, wl.W, wl.residual)
@@ -78,3 +78,60 @@ def test_fwd_repeated_calls_are_identical():
     a = dsc.lowrank_fwd(inp["x"], inp["z"], inp["U"], 1, 4, True)
     b = dsc.lowrank_fwd(inp["x"], inp["z"], inp["U"], 1, 4, True)
     assert torch.equal(a, b)
+
+
+def run_bwd(wl, seed):
+    assert dsc.dsc_lowrank_uses_tensor_cores(wl.B, wl.T, wl.C, wl.H, wl.W, wl.R, wl.dtype) & 2
+    inp = syn.make_inputs(wl, seed, device="cuda")
+    x, z, U, dy = inp["x"], inp["z"], inp["U"], inp["dy"]
+    dx, dz, dU = Guarded(x.shape, wl.dtype), Guarded(z.shape, wl.dtype), Guarded(U.shape, wl.dtype)
+    ws = dsc.lowrank_workspace(x, z, wl.H, wl.W)
+    ws.fill_(0x5A)                      # workspace contents on entry must not matter
+    dsc.dsc_lowrank_bwd(x, z, U, dy, dx.t, dz.t, dU.t, ws, wl.H, wl.W, wl.residual)
+    torch.cuda.synchronize()
+    for o, n in ((dx, "dx"), (dz, "dz"), (dU, "dU")):
+        assert o.guards_intact(), f"{n}: write outside the tensor"
+    rdx, rdz, rdU = orc.lowrank_bwd(x, z, U, dy, wl.H, wl.W, wl.residual)
+    assert_grad(dx.t, rdx, wl.dtype, "dx")
+    assert_grad(dz.t, rdz, wl.dtype, "dz")
+    assert_grad(dU.t, rdU, wl.dtype, "dU")
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+def test_bwd_every_width(W):
+    wl = syn.Workload("tc_bwd", B=2, T=300, C=320, W=W, H=1, R=16, residual=True)
+    run_bwd(wl, seed=20 + W)
+
+
+@pytest.mark.parametrize("residual", [False, True])
+def test_bwd_residual_flag(residual):
+    wl = syn.Workload("tc_bwd_res", B=3, T=257, C=192, W=4, H=1, R=16, residual=residual)
+    run_bwd(wl, seed=4)
+
+
+@pytest.mark.parametrize("T", [1, 3, 4, 127, 128, 129, 131])
+def test_bwd_short_and_ragged_sequences(T):
+    wl = syn.Workload("tc_bwd_T", B=3, T=T, C=128, W=4, H=1, R=16)
+    run_bwd(wl, seed=100 + T)
+
+
+@pytest.mark.parametrize("C", [8, 24, 72, 136, 200])
+def test_bwd_channels_not_a_multiple_of_the_chunk(C):
+    wl = syn.Workload("tc_bwd_C", B=2, T=150, C=C, W=4, H=1, R=16)
+    run_bwd(wl, seed=200 + C)
+
+
+def test_bwd_many_chunks_per_cta_and_many_tiles_per_split():
+    # several channel chunks per CTA (dU accumulators handed over between
+    # chunks) and several token tiles per split (dz accumulators per tile)
+    wl = syn.Workload("tc_bwd_big", B=4, T=1024, C=4096, W=4, H=1, R=16)
+    run_bwd(wl, seed=88)
+
+
+def test_bwd_repeated_calls_are_identical():
+    wl = syn.Workload("tc_bwd_det", B=2, T=640, C=1024, W=4, H=1, R=16)
+    inp = syn.make_inputs(wl, 6, device="cuda")
+    a = dsc.lowrank_bwd(inp["x"], inp["z"], inp["U"], inp["dy"], 1, 4, True)
+    b = dsc.lowrank_bwd(inp["x"], inp["z"], inp["U"], inp["dy"], 1, 4, True)
+    for p, q in zip(a, b):
+        assert torch.equal(p, q)

@@ -60,7 +60,7 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
 
 def test_noalloc_refuses_a_problem_larger_than_its_scratch():
     f = noalloc_entry()
-    B, T, C, H, W, R = 8, 2048, 6144, 1, 4, 16
+    B, T, C, H, W, R = 32, 2048, 6144, 1, 4, 16       # 64 Ki tokens at the QKV width
     need = dsc.dsc_lowrank_bwd_workspace_size(B, T, C, H, W, R, torch.bfloat16)
     assert need > MAX_BYTES
     # Refused during the size check, before any pointer is used or work enqueued.
