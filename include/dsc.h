@@ -149,7 +149,8 @@ int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H,
  * Diagnostic: the device error word of the tensor-core kernels on the
  * current device.  0 means no error; otherwise it holds the code of the
  * first bounded wait that gave up (1 producer, 2 MMA issuer, 3 epilogue,
- * 4 store), after which that kernel returned early and its outputs are
+ * 4 store, 5 second MMA issuer), after which that kernel returned early and
+ * its outputs are
  * invalid.  `reset` != 0 clears the word.  Synchronous (it copies one word
  * from the device); not meant for the hot path.
  */

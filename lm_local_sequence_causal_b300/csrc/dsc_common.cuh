@@ -127,6 +127,60 @@ __device__ __forceinline__ void load_chunk(const T* __restrict__ p, float (&out)
   }
 }
 
+// The same `n` elements held as raw bits, so a load can be issued early
+// (prefetched) and decoded to fp32 later.  Same alignment rule as above.
+template <typename T, int n>
+struct RawChunk {
+  static constexpr int bytes = n * (int)sizeof(T);
+  static constexpr int vb = (bytes % 16 == 0) ? 16 : (bytes % 8 == 0) ? 8
+                          : (bytes % 4 == 0) ? 4 : (int)sizeof(T);
+  static constexpr int per = vb / (int)sizeof(T);   // elements per access
+  static constexpr int cnt = n / per;                // accesses
+  static constexpr int words = vb >= 4 ? vb / 4 : 1; // 32-bit words per access
+  uint32_t w[cnt][words];
+
+  __device__ __forceinline__ void load(const T* __restrict__ p) {
+#pragma unroll
+    for (int i = 0; i < cnt; ++i) {
+      const T* q = p + i * per;
+      if constexpr (vb == 16) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(q));
+        w[i][0] = u.x; w[i][1] = u.y; w[i][2] = u.z; w[i][3] = u.w;
+      } else if constexpr (vb == 8) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(q));
+        w[i][0] = u.x; w[i][1] = u.y;
+      } else if constexpr (vb == 4) {
+        w[i][0] = __ldg(reinterpret_cast<const unsigned int*>(q));
+      } else {
+        w[i][0] = __ldg(reinterpret_cast<const unsigned short*>(q));
+      }
+    }
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < cnt; ++i)
+#pragma unroll
+      for (int j = 0; j < words; ++j) w[i][j] = 0u;
+  }
+  __device__ __forceinline__ void unpack(float (&out)[n]) const {
+#pragma unroll
+    for (int i = 0; i < cnt; ++i) {
+      if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int e = 0; e < per; ++e) out[i * per + e] = __uint_as_float(w[i][e]);
+      } else if constexpr (vb >= 4) {
+#pragma unroll
+        for (int e = 0; e < per / 2; ++e) {
+          out[i * per + 2 * e] = __uint_as_float(w[i][e] << 16);
+          out[i * per + 2 * e + 1] = __uint_as_float(w[i][e] & 0xffff0000u);
+        }
+      } else {
+        out[i] = __uint_as_float(w[i][0] << 16);
+      }
+    }
+  }
+};
+
 // Store `n` consecutive fp32 values as T, widest aligned access (see above).
 template <typename T, int n>
 __device__ __forceinline__ void store_chunk(T* __restrict__ p, const float (&v)[n]) {

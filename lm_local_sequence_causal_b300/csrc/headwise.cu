@@ -22,6 +22,7 @@
 // adjacent lanes and reduce dw by butterfly shuffles).  Every other H runs a
 // plain per-channel path that is correct but not tuned.
 #include <algorithm>
+#include <mutex>
 
 #include "dsc_common.cuh"
 #include "dsc_internal.h"
@@ -31,19 +32,30 @@ namespace {
 
 constexpr int kThreads = 128;
 
-// The grid is one-dimensional over (sequence b, token tile, channel block),
-// channel block fastest, so any B and T fit the launch limits.
-struct Tile {
-  int64_t cb, tt, b;
+// Work split: the B*T tokens are one flat axis n = b*T + t.  The grid is
+// (channel block of 128 threads) x (token range); ranges are contiguous and
+// balanced to +-1 token, and the grid is sized to the CTAs that fit on the
+// GPU at once, so every CTA streams the same number of rows and there is no
+// partial last wave.  A range may cross sequence boundaries: at t = 0 the
+// causal window restarts from zero, and a tap only links rows of the same
+// sequence.
+
+// Tokens of look-ahead: each thread keeps the loads of the next kPF tokens
+// in flight (a register ring), so a CTA has about kPF x 24-40 bytes per
+// thread outstanding -- enough, at a few CTAs per SM, to cover HBM latency.
+constexpr int kPF = 4;    // forward (x and the taps: 24 bytes a token)
+constexpr int kPFB = 4;   // backward (dy, taps and x: 40 bytes a token)
+
+struct Range {
+  int64_t cb, n0, n1;
 };
-__device__ __forceinline__ Tile decode_tile(int64_t ncb, int64_t ntt) {
-  int64_t i = blockIdx.x;
-  Tile t;
-  t.cb = i % ncb;
-  i /= ncb;
-  t.tt = i % ntt;
-  t.b = i / ntt;
-  return t;
+__device__ __forceinline__ Range decode_range(int64_t ncb, int64_t nranges, int64_t N) {
+  Range r;
+  r.cb = blockIdx.x % ncb;
+  const int64_t i = blockIdx.x / ncb;
+  r.n0 = N * i / nranges;
+  r.n1 = N * (i + 1) / nranges;
+  return r;
 }
 
 // ------------------------------------------------------------ forward ----
@@ -51,76 +63,101 @@ __device__ __forceinline__ Tile decode_tile(int64_t ncb, int64_t ntt) {
 template <typename T, int W, int NG>
 __global__ void __launch_bounds__(kThreads)
 hw_fwd_kernel(const T* __restrict__ x, const T* __restrict__ w, T* __restrict__ y,
-              int64_t Tlen, int64_t C, int64_t H, int residual, int L, int64_t ncb,
-              int64_t ntt) {
+              int64_t Tlen, int64_t C, int64_t H, int residual, int64_t N, int64_t ncb,
+              int64_t nranges) {
   constexpr int V = Vec<T>::N;
-  const Tile tl = decode_tile(ncb, ntt);
-  const int64_t cv = tl.cb * blockDim.x + threadIdx.x;
+  const Range rg = decode_range(ncb, nranges, N);
+  const int64_t cv = rg.cb * blockDim.x + threadIdx.x;
   const int64_t c0 = cv * V;
   if (c0 >= C) return;
   const int64_t G = C / H;
-  const int64_t b = tl.b;
-  const int64_t t0 = tl.tt * L;
-  const int64_t t1 = t0 + L < Tlen ? t0 + L : Tlen;
-  const T* xb = x + b * Tlen * C + c0;
-  const T* wb = w + b * Tlen * G * W + (c0 / H) * W;
-  T* yb = y + b * Tlen * C + c0;
+  const int64_t n0 = rg.n0, n1 = rg.n1;
+  const T* xb = x + c0;
+  const T* wb = w + (c0 / H) * W;
+  T* yb = y + c0;
 
-  float win[W > 1 ? W - 1 : 1][V];  // win[j] = x[t-1-j]
+  int64_t t = n0 % Tlen;             // position of token n in its sequence
+  float win[W > 1 ? W - 1 : 1][V];   // win[j] = x[n-1-j] (zero before the sequence start)
 #pragma unroll
   for (int j = 0; j < W - 1; ++j) {
-    const int64_t t = t0 - 1 - j;
-    if (t >= 0) {
-      unpack16<T>(ldg16(xb + t * C), win[j]);
+    if (t - 1 - j >= 0) {
+      unpack16<T>(ldg16(xb + (n0 - 1 - j) * C), win[j]);
     } else {
 #pragma unroll
       for (int v = 0; v < V; ++v) win[j][v] = 0.f;
     }
   }
 
-#pragma unroll 2
-  for (int64_t t = t0; t < t1; ++t) {
-    float xv[V];
-    unpack16<T>(ldg16(xb + t * C), xv);
-    float taps[NG * W];
-    load_chunk<T, NG * W>(wb + t * G * W, taps);
-    float out[V];
+  uint4 xr[kPF];
+  RawChunk<T, NG * W> wr[kPF];
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const int gi = NG == 1 ? 0 : v / (V / NG);
-      float a = residual ? xv[v] : 0.f;
-      a = fmaf(taps[gi * W], xv[v], a);
-#pragma unroll
-      for (int k = 1; k < W; ++k) a = fmaf(taps[gi * W + k], win[k - 1][v], a);
-      out[v] = a;
+  for (int j = 0; j < kPF; ++j) {
+    if (n0 + j < n1) {
+      xr[j] = ldg16(xb + (n0 + j) * C);
+      wr[j].load(wb + (n0 + j) * G * W);
     }
-    stcs16(yb + t * C, pack16<T>(out));
+  }
+  for (int64_t nb = n0; nb < n1; nb += kPF) {
 #pragma unroll
-    for (int j = W - 2; j > 0; --j)
+    for (int j = 0; j < kPF; ++j) {
+      const int64_t n = nb + j;
+      if (n < n1) {
+        if (t == 0) {
 #pragma unroll
-      for (int v = 0; v < V; ++v) win[j][v] = win[j - 1][v];
-    if constexpr (W > 1) {
+          for (int q = 0; q < W - 1; ++q)
 #pragma unroll
-      for (int v = 0; v < V; ++v) win[0][v] = xv[v];
+            for (int v = 0; v < V; ++v) win[q][v] = 0.f;
+        }
+        float xv[V];
+        unpack16<T>(xr[j], xv);
+        float taps[NG * W];
+        wr[j].unpack(taps);
+        if (n + kPF < n1) {
+          xr[j] = ldg16(xb + (n + kPF) * C);
+          wr[j].load(wb + (n + kPF) * G * W);
+        }
+        float out[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          const int gi = NG == 1 ? 0 : v / (V / NG);
+          float a = residual ? xv[v] : 0.f;
+          a = fmaf(taps[gi * W], xv[v], a);
+#pragma unroll
+          for (int k = 1; k < W; ++k) a = fmaf(taps[gi * W + k], win[k - 1][v], a);
+          out[v] = a;
+        }
+        stcs16(yb + n * C, pack16<T>(out));
+#pragma unroll
+        for (int q = W - 2; q > 0; --q)
+#pragma unroll
+          for (int v = 0; v < V; ++v) win[q][v] = win[q - 1][v];
+        if constexpr (W > 1) {
+#pragma unroll
+          for (int v = 0; v < V; ++v) win[0][v] = xv[v];
+        }
+        if (++t == Tlen) t = 0;
+      }
     }
   }
 }
 
 // ----------------------------------------------------------- backward ----
 
-// One token step of the backward sweep is described in the file comment; the
-// loop runs t over [t0, t1 + W - 1): step t adds the contributions of dy[t]
-// to dx rows t-W+1..t (scatter form, so no filter row is kept), forms dw[t]
-// when t is inside the tile, and retires dx row t-W+1.
+// One step n of the backward sweep (scatter form, so no filter row is kept):
+// dy[n] feeds the dx rows n-k of the same sequence through tap k, dw[n] is
+// formed when n is inside the range, and dx row n-W+1 is retired.  The steps
+// run over [n0, n1 + W - 1) (cut at N), so the last rows of the range get
+// the contributions of the next W-1 tokens.  The dy, w and x rows of the
+// next kPF steps are in flight while a step computes.
 template <typename T, int W, int NG>
 __global__ void __launch_bounds__(kThreads)
 hw_bwd_kernel(const T* __restrict__ x, const T* __restrict__ w,
               const T* __restrict__ dy, T* __restrict__ dx, T* __restrict__ dw,
-              int64_t Tlen, int64_t C, int64_t H, int residual, int L, int tpg, int64_t ncb,
-              int64_t ntt) {
+              int64_t Tlen, int64_t C, int64_t H, int residual, int tpg, int64_t N,
+              int64_t ncb, int64_t nranges) {
   constexpr int V = Vec<T>::N;
-  const Tile tl = decode_tile(ncb, ntt);
-  const int64_t cv = tl.cb * blockDim.x + threadIdx.x;
+  const Range rg = decode_range(ncb, nranges, N);
+  const int64_t cv = rg.cb * blockDim.x + threadIdx.x;
   const int64_t nvec = C / V;
   // Lanes past the channel range leave together with their whole group
   // (C % H == 0), so the shuffle mask is the prefix of active lanes.
@@ -130,20 +167,22 @@ hw_bwd_kernel(const T* __restrict__ x, const T* __restrict__ w,
   if (cv >= nvec) return;
   const int64_t c0 = cv * V;
   const int64_t G = C / H;
-  const int64_t b = tl.b;
-  const int64_t t0 = tl.tt * L;
-  const int64_t t1 = t0 + L < Tlen ? t0 + L : Tlen;
-  const int64_t base = b * Tlen * C + c0;
-  const int64_t wbase = b * Tlen * G * W + (c0 / H) * W;
+  const int64_t n0 = rg.n0, n1 = rg.n1;
+  const int64_t wrow = G * W;
+  const T* xb = x + c0;
+  const T* gb = dy + c0;
+  const T* wb = w + (c0 / H) * W;
+  T* dxb = dx + c0;
+  T* dwb = dw + (c0 / H) * W;
   const bool leader = (NG > 1) || ((cv & (tpg - 1)) == 0);
 
-  float xwin[W > 1 ? W - 1 : 1][V];  // x[t-1-j]
-  float acc[W][V];                   // acc[j] = dx row t-(W-1)+j
+  int64_t t = n0 % Tlen;
+  float xwin[W > 1 ? W - 1 : 1][V];  // x[n-1-j], zero before the sequence start
+  float acc[W][V];                   // acc[j] = dx row n-(W-1)+j
 #pragma unroll
   for (int j = 0; j < W - 1; ++j) {
-    const int64_t t = t0 - 1 - j;
-    if (t >= 0) {
-      unpack16<T>(ldg16(x + base + t * C), xwin[j]);
+    if (t - 1 - j >= 0) {
+      unpack16<T>(ldg16(xb + (n0 - 1 - j) * C), xwin[j]);
     } else {
 #pragma unroll
       for (int v = 0; v < V; ++v) xwin[j][v] = 0.f;
@@ -154,67 +193,102 @@ hw_bwd_kernel(const T* __restrict__ x, const T* __restrict__ w,
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[j][v] = 0.f;
 
-  const int64_t tend = t1 + W - 1;
-#pragma unroll 2
-  for (int64_t t = t0; t < tend; ++t) {
-    float g[V];
-    float taps[NG * W];
-    if (t < Tlen) {
-      unpack16<T>(ldg16(dy + base + t * C), g);
-      load_chunk<T, NG * W>(w + wbase + t * G * W, taps);
-    } else {
+  const int64_t nend = n1 + W - 1 < N ? n1 + W - 1 : N;
+  uint4 gr[kPFB], xr[kPFB];
+  RawChunk<T, NG * W> wr[kPFB];
 #pragma unroll
-      for (int v = 0; v < V; ++v) g[v] = 0.f;
-#pragma unroll
-      for (int i = 0; i < NG * W; ++i) taps[i] = 0.f;
+  for (int j = 0; j < kPFB; ++j) {
+    const int64_t n = n0 + j;
+    if (n < nend) {
+      gr[j] = ldg16(gb + n * C);
+      wr[j].load(wb + n * wrow);
     }
-    // dx: row t enters the window; dy[t] feeds rows t-k through tap k.
+    if (n < n1) xr[j] = ldg16(xb + n * C);
+  }
+  for (int64_t nb = n0; nb < nend; nb += kPFB) {
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[W - 1][v] = (residual && t < t1) ? g[v] : 0.f;
+    for (int jj = 0; jj < kPFB; ++jj) {
+      const int64_t n = nb + jj;
+      if (n < nend) {
+        const bool inside = n < n1;
+        float g[V];
+        unpack16<T>(gr[jj], g);
+        float taps[NG * W];
+        wr[jj].unpack(taps);
+        float xv[V];
+        if (inside) unpack16<T>(xr[jj], xv);
+        const int64_t nn = n + kPFB;
+        if (nn < nend) {
+          gr[jj] = ldg16(gb + nn * C);
+          wr[jj].load(wb + nn * wrow);
+        }
+        if (nn < n1) xr[jj] = ldg16(xb + nn * C);
+        // dx: row n enters the window; dy[n] feeds rows n-k (same sequence).
 #pragma unroll
-    for (int k = 0; k < W; ++k) {
+        for (int v = 0; v < V; ++v) acc[W - 1][v] = (residual && inside) ? g[v] : 0.f;
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
-        const int gi = NG == 1 ? 0 : v / (V / NG);
-        acc[W - 1 - k][v] = fmaf(taps[gi * W + k], g[v], acc[W - 1 - k][v]);
+        for (int k = 0; k < W; ++k) {
+          if (t >= k) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+              const int gi = NG == 1 ? 0 : v / (V / NG);
+              acc[W - 1 - k][v] = fmaf(taps[gi * W + k], g[v], acc[W - 1 - k][v]);
+            }
+          }
+        }
+        if (inside) {
+          if (t == 0) {
+#pragma unroll
+            for (int q = 0; q < W - 1; ++q)
+#pragma unroll
+              for (int v = 0; v < V; ++v) xwin[q][v] = 0.f;
+          }
+          // dw[n, g, k] = sum over the group's channels of dy[n,c] x[n-k,c].
+          float p[NG * W];
+#pragma unroll
+          for (int i = 0; i < NG * W; ++i) p[i] = 0.f;
+#pragma unroll
+          for (int v = 0; v < V; ++v) {
+            const int gi = NG == 1 ? 0 : v / (V / NG);
+            p[gi * W] = fmaf(g[v], xv[v], p[gi * W]);
+#pragma unroll
+            for (int k = 1; k < W; ++k)
+              p[gi * W + k] = fmaf(g[v], xwin[k - 1][v], p[gi * W + k]);
+          }
+          if constexpr (NG == 1) {
+            for (int off = 1; off < tpg; off <<= 1)
+#pragma unroll
+              for (int k = 0; k < W; ++k) p[k] += __shfl_xor_sync(mask, p[k], off);
+          }
+          if (leader) store_chunk<T, NG * W>(dwb + n * wrow, p);
+#pragma unroll
+          for (int q = W - 2; q > 0; --q)
+#pragma unroll
+            for (int v = 0; v < V; ++v) xwin[q][v] = xwin[q - 1][v];
+          if constexpr (W > 1) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) xwin[0][v] = xv[v];
+          }
+        }
+        // dx row n-W+1 has received every contribution.
+        const int64_t sr = n - (W - 1);
+        if (sr >= n0) stcs16(dxb + sr * C, pack16<T>(acc[0]));
+#pragma unroll
+        for (int q = 0; q < W - 1; ++q)
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[q][v] = acc[q + 1][v];
+        if (++t == Tlen) t = 0;
       }
     }
-    if (t < t1) {
-      // dw[t, g, k] = sum over the group's channels of dy[t,c] x[t-k,c].
-      float xv[V];
-      unpack16<T>(ldg16(x + base + t * C), xv);
-      float p[NG * W];
+  }
+  // If the sweep stopped at the end of the data, the last W-1 rows are still
+  // in the window; they are complete, so retire them here.
+  if (nend < n1 + W - 1) {
 #pragma unroll
-      for (int i = 0; i < NG * W; ++i) p[i] = 0.f;
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        const int gi = NG == 1 ? 0 : v / (V / NG);
-        p[gi * W] = fmaf(g[v], xv[v], p[gi * W]);
-#pragma unroll
-        for (int k = 1; k < W; ++k) p[gi * W + k] = fmaf(g[v], xwin[k - 1][v], p[gi * W + k]);
-      }
-      if constexpr (NG == 1) {
-        for (int off = 1; off < tpg; off <<= 1)
-#pragma unroll
-          for (int k = 0; k < W; ++k) p[k] += __shfl_xor_sync(mask, p[k], off);
-      }
-      if (leader) store_chunk<T, NG * W>(dw + wbase + t * G * W, p);
-#pragma unroll
-      for (int j = W - 2; j > 0; --j)
-#pragma unroll
-        for (int v = 0; v < V; ++v) xwin[j][v] = xwin[j - 1][v];
-      if constexpr (W > 1) {
-#pragma unroll
-        for (int v = 0; v < V; ++v) xwin[0][v] = xv[v];
-      }
+    for (int j = 0; j < W - 1; ++j) {
+      const int64_t sr = nend - (W - 1) + j;
+      if (sr >= n0 && sr < n1) stcs16(dxb + sr * C, pack16<T>(acc[j]));
     }
-    // dx row t-W+1 has received every contribution.
-    const int64_t s = t - (W - 1);
-    if (s >= t0) stcs16(dx + base + s * C, pack16<T>(acc[0]));
-#pragma unroll
-    for (int j = 0; j < W - 1; ++j)
-#pragma unroll
-      for (int v = 0; v < V; ++v) acc[j][v] = acc[j + 1][v];
   }
 }
 
@@ -270,13 +344,38 @@ __global__ void hw_dw_generic(const T* __restrict__ x, const T* __restrict__ dy,
 
 // ------------------------------------------------------------ dispatch ----
 
-// Tokens per tile: long enough to amortise the W-1 row halo, short enough
-// to give every SM several CTAs.
-int tile_len(const Shape& s, int64_t ctas_x) {
-  int64_t L = 64;
-  while (L > 16 && ctas_x * s.B * ((s.T + L - 1) / L) < 4 * 148) L /= 2;
-  while (ctas_x * s.B * ((s.T + L - 1) / L) > (int64_t(1) << 30)) L *= 2;
-  return (int)L;
+// Token ranges for a grid of `ncb` channel blocks: as many CTAs as fit on
+// the GPU at once (occupancy of this kernel x SMs), at least 16 tokens each.
+// Resident CTAs per SM of `kernel` at `threads` threads, cached per kernel
+// (keyed by its address: every instance of one template shares a type).
+int blocks_per_sm(const void* kernel, int threads) {
+  static std::mutex mu;
+  static const void* keys[64] = {};
+  static int vals[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < 64; ++i) {
+    if (keys[i] == kernel) return vals[i];
+    if (keys[i] == nullptr) {
+      int nb = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess ||
+          nb <= 0)
+        nb = 2;
+      keys[i] = kernel;
+      vals[i] = nb;
+      return nb;
+    }
+  }
+  return 2;
+}
+
+// Token ranges for a grid of `ncb` channel blocks: as many CTAs as fit on
+// the GPU at once (occupancy of this kernel x SMs), at least 16 tokens each.
+int64_t n_ranges(const void* kernel, int threads, int64_t ncb, int64_t N) {
+  const int per_sm = blocks_per_sm(kernel, threads);
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  int64_t r = std::max<int64_t>(1, static_cast<int64_t>(per_sm) * sms / ncb);
+  r = std::min<int64_t>(r, std::max<int64_t>(1, N / 16));
+  return std::min<int64_t>(r, (int64_t(1) << 31) / ncb - 1);
 }
 
 template <typename T>
@@ -320,13 +419,14 @@ cudaError_t fwd_t(const void* x, const void* w, void* y, const Shape& s, cudaStr
   const int64_t nvec = s.C / V;
   const int threads = (int)std::min<int64_t>(kThreads, (nvec + 31) / 32 * 32);
   const int64_t gx = (nvec + threads - 1) / threads;
-  const int L = tile_len(s, gx);
-  const int64_t ntt = (s.T + L - 1) / L;
-  const unsigned grid = (unsigned)(gx * ntt * s.B);
+  const int64_t N = s.N();
   DSC_W_SWITCH(s.W, DSC_NG_SWITCH(ng, {
-    if constexpr (NG_ <= V)
-      hw_fwd_kernel<T, W_, NG_><<<grid, threads, 0, st>>>(
-          (const T*)x, (const T*)w, (T*)y, s.T, s.C, s.H, s.residual, L, gx, ntt);
+    if constexpr (NG_ <= V) {
+      auto kern = hw_fwd_kernel<T, W_, NG_>;
+      const int64_t nr = n_ranges((const void*)kern, threads, gx, N);
+      kern<<<(unsigned)(gx * nr), threads, 0, st>>>((const T*)x, (const T*)w, (T*)y, s.T, s.C,
+                                                    s.H, s.residual, N, gx, nr);
+    }
   }))
   return cudaGetLastError();
 }
@@ -350,15 +450,16 @@ cudaError_t bwd_t(const void* x, const void* w, const void* dy, void* dx, void* 
   const int64_t nvec = s.C / V;
   const int threads = (int)std::min<int64_t>(kThreads, (nvec + 31) / 32 * 32);
   const int64_t gx = (nvec + threads - 1) / threads;
-  const int L = tile_len(s, gx);
   const int tpg = ng == 1 ? (int)(s.H / V) : 1;
-  const int64_t ntt = (s.T + L - 1) / L;
-  const unsigned grid = (unsigned)(gx * ntt * s.B);
+  const int64_t N = s.N();
   DSC_W_SWITCH(s.W, DSC_NG_SWITCH(ng, {
-    if constexpr (NG_ <= V)
-      hw_bwd_kernel<T, W_, NG_><<<grid, threads, 0, st>>>(
-          (const T*)x, (const T*)w, (const T*)dy, (T*)dx, (T*)dw, s.T, s.C, s.H,
-          s.residual, L, tpg, gx, ntt);
+    if constexpr (NG_ <= V) {
+      auto kern = hw_bwd_kernel<T, W_, NG_>;
+      const int64_t nr = n_ranges((const void*)kern, threads, gx, N);
+      kern<<<(unsigned)(gx * nr), threads, 0, st>>>((const T*)x, (const T*)w, (const T*)dy,
+                                                    (T*)dx, (T*)dw, s.T, s.C, s.H, s.residual,
+                                                    tpg, N, gx, nr);
+    }
   }))
   return cudaGetLastError();
 }

@@ -22,9 +22,11 @@
 //   warp 1      allocates 512 TMEM columns; one lane issues the MMAs
 //               (M = 128, N = 64*W, K = 16 per instruction) into one of two
 //               TMEM accumulators and commits them to mbarriers.
-//   warps 2-9   epilogue: warp (w % 4) owns TMEM lanes 32*(w % 4) .. +31 =
-//               those tokens; warps 2-5 take channels 0-31 of the chunk,
-//               warps 6-9 channels 32-63.  Each thread loads its token's
+//   warps 2-17  epilogue, two groups of 8 warps taking alternate items (each
+//               with its own TMEM accumulator and y staging buffer, so the
+//               groups overlap); in a group, warp (w % 4) owns TMEM lanes
+//               32*(w % 4) .. +31 = those tokens and the two warps of each
+//               lane group split the chunk's channels.  Each thread loads its token's
 //               W taps for 8 channels at a time (tcgen05.ld), reads
 //               x[t-k] for the same 8 channels from the staged tile (16-byte
 //               swizzled reads, no bank conflicts), forms
@@ -54,14 +56,20 @@ namespace {
 using namespace sm100;
 
 // Set when a bounded wait gives up: 1 = producer, 2 = MMA issuer,
-// 3 = epilogue, 4 = y store.  Cleared only by lowrank_tc_error(reset).
+// 3 = epilogue, 4 = y store, 5 = second MMA issuer (backward dz/dU).
+// Cleared only by lowrank_tc_error(reset).
 __device__ unsigned int g_tc_error = 0;
 
 constexpr int BM = 128;     // tokens per tile = TMEM lanes
 constexpr int CC = 64;      // channels per chunk = one 128-byte swizzled row
 constexpr int NST = 4;      // input pipeline stages
-constexpr int NEPI = 8;     // epilogue warps
-constexpr int kFwdThreads = (2 + NEPI) * 32;
+constexpr int NEPI_F = 16;  // forward epilogue warps: two groups of 8 that take alternate items
+constexpr int NGRP = 8;     // warps per forward epilogue group (4 lane groups x 2 channel halves)
+constexpr int kFwdThreads = (2 + NEPI_F) * 32;
+constexpr int NEPI = 8;     // warps per backward epilogue group (4 lane groups x 2 channel halves)
+// producer, D-MMA issuer, dx group, dw group, dz/dU-MMA issuer
+constexpr int kBwdThreads = (3 + 2 * NEPI) * 32;
+constexpr int kDzduWarp = 2 + 2 * NEPI;
 constexpr uint32_t kTmemCols = 512;
 
 __host__ __device__ constexpr int round1k(int b) { return (b + 1023) / 1024 * 1024; }
@@ -72,19 +80,20 @@ struct FwdLayout {
   static constexpr int XBOX = XROWS * 128;            // bytes of one x box
   static constexpr int XBYTES = round1k(XBOX);
   static constexpr int ZBYTES = BM * 32;              // one K-step of z (4 KB)
-  static constexpr int NCOL = CC * W;                 // MMA N
-  static constexpr int BBYTES = round1k(NCOL * 32);   // one K-step of U
-  static constexpr int YBYTES = BM * 128;
-  static constexpr int X_OFF = 0;
-  static constexpr int Z_OFF = X_OFF + NST * XBYTES;
-  static constexpr int B_OFF = Z_OFF + NST * KS * ZBYTES;
-  static constexpr int Y_OFF = B_OFF + 2 * KS * BBYTES;
+  static constexpr int NCOL = CC * W;                 // MMA N (U columns of the chunk)
+  static constexpr int UATOM = KS * 16 * 128;         // 64 U columns x R rows (2 or 4 KB)
+  static constexpr int UBYTES = W * UATOM;
+  static constexpr int STAGE = XBYTES + KS * ZBYTES + round1k(UBYTES);
+  static constexpr int YBYTES = BM * 128;             // staged y tile of one group
+  static constexpr int Z_IN = XBYTES;                 // offsets inside a stage
+  static constexpr int U_IN = XBYTES + KS * ZBYTES;
+  static constexpr int Y_OFF = NST * STAGE;
   static constexpr int BAR_OFF = Y_OFF + 2 * YBYTES;
   // full[NST] empty[NST] accf[2] acce[2] yfull[2] yfree[2]
   static constexpr int NBAR = 2 * NST + 8;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int TOTAL = MISC_OFF + 16 + 1024;  // + slack to align the base
-  static constexpr uint32_t TX = XBOX + KS * ZBYTES;  // bytes landing per stage
+  static constexpr uint32_t TX = XBOX + KS * ZBYTES + UBYTES;  // bytes landing per stage
 };
 
 __device__ __forceinline__ unsigned char* align1k(unsigned char* p) {
@@ -92,36 +101,32 @@ __device__ __forceinline__ unsigned char* align1k(unsigned char* p) {
                                           ~static_cast<uintptr_t>(1023));
 }
 
+// Work item i of the forward -> (b, token tile, chunk): tile-major, so the
+// CTAs working side by side (items i, i+1, ... handed out round-robin) read
+// neighbouring 128-byte pieces of the same rows of x.
 struct Item {
   int chunk, b, t0;
 };
-__device__ __forceinline__ Item decode(long long i, int nbt, int ntiles) {
+__device__ __forceinline__ Item decode_tm(long long i, int nchunks, int ntiles) {
   Item it;
-  it.chunk = static_cast<int>(i / nbt);
-  const int rem = static_cast<int>(i - static_cast<long long>(it.chunk) * nbt);
-  it.b = rem / ntiles;
-  it.t0 = (rem - it.b * ntiles) * BM;
+  const long long tile = i / nchunks;
+  it.chunk = static_cast<int>(i - tile * nchunks);
+  it.b = static_cast<int>(tile / ntiles);
+  it.t0 = static_cast<int>(tile - static_cast<long long>(it.b) * ntiles) * BM;
   return it;
 }
 
-// Fill the K-major 32-byte-swizzled B operand of chunk `chunk`: row n (the
-// chunk's column c*W + k), K-element r = U[r, chunk*64*W + n] (zero past R
-// or past the channel count).
-template <int W, int KS>
-__device__ void fill_u_tile(unsigned char* dst, const __nv_bfloat16* __restrict__ U, int chunk,
-                            int C, int R) {
-  using L = FwdLayout<W, KS>;
-  const int64_t GW = static_cast<int64_t>(C) * W;
-  for (int idx = threadIdx.x; idx < KS * L::NCOL * 16; idx += blockDim.x) {
-    const int ks = idx / (L::NCOL * 16);
-    const int rem = idx - ks * L::NCOL * 16;
-    const int n = rem >> 4, k = rem & 15;
-    const int r = ks * 16 + k;
-    const int64_t col = static_cast<int64_t>(chunk) * L::NCOL + n;
-    __nv_bfloat16 v = __float2bfloat16_rn(0.f);
-    if (r < R && col < GW) v = U[static_cast<int64_t>(r) * GW + col];
-    *reinterpret_cast<__nv_bfloat16*>(dst + ks * L::BBYTES + sw32_offset(n, k)) = v;
-  }
+// fp32 pairs for the packed FMA (fma.rn.f32x2).
+__device__ __forceinline__ float2 f2(uint32_t lo, uint32_t hi) {
+  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
+// The two bf16 of a 32-bit word as an fp32 pair (exact).
+__device__ __forceinline__ float2 bf2f(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t f2bf(float2 v) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 // Wait for a phase during teardown: ignores the abort flag, bounded in time.
@@ -132,11 +137,27 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (globaltimer() - t0 > kWaitLimitNs) return;
 }
 
+// Shared-memory descriptor (fields as in sm100.cuh); layout 0 = no swizzle
+// (8-row x 16-byte core matrices), 2 = 128-byte swizzle, 6 = 32-byte swizzle.
+__device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(layout) << 61);
+}
+
+// kind::f16 instruction descriptor with operand majors (0 = K-major, 1 = MN-major).
+__host__ __device__ constexpr uint32_t idesc_major(uint32_t M, uint32_t N, uint32_t amaj,
+                                                   uint32_t bmaj) {
+  return idesc_bf16_f32(M, N) | (amaj << 15) | (bmaj << 16);
+}
+
 template <int W, int KS>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
-          const __grid_constant__ CUtensorMap tm_y, const __nv_bfloat16* __restrict__ U, int C,
-          int R, int ntiles, int nbt, int nchunks, int residual) {
+          const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_y,
+          int ntiles, int nbt, int nchunks, int residual) {
   using L = FwdLayout<W, KS>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1k(smem_raw);
@@ -144,8 +165,10 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const long long items = static_cast<long long>(nchunks) * nbt;
-  const long long i0 = items * blockIdx.x / gridDim.x;
-  const long long i1 = items * (blockIdx.x + 1) / gridDim.x;
+  // this CTA's items: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int nmine = items > blockIdx.x
+                        ? static_cast<int>((items - 1 - blockIdx.x) / gridDim.x) + 1
+                        : 0;
 
   const uint32_t bar_full = sb + L::BAR_OFF;
   const uint32_t bar_empty = bar_full + NST * 8;
@@ -159,28 +182,22 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1 + NEPI);
+      mbar_init(bar_empty + 8 * s, 1 + NGRP);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_accf + 8 * a, 1);
-      mbar_init(bar_acce + 8 * a, NEPI);
-      mbar_init(bar_yfull + 8 * a, NEPI);
+      mbar_init(bar_acce + 8 * a, NGRP);
+      mbar_init(bar_yfull + 8 * a, NGRP);
       mbar_init(bar_yfree + 8 * a, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_z);
+    tma_prefetch_desc(&tm_u);
     tma_prefetch_desc(&tm_y);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-
-  const int chunk_first = i1 > i0 ? static_cast<int>(i0 / nbt) : 0;
-  const int chunk_last = i1 > i0 ? static_cast<int>((i1 - 1) / nbt) : -1;
-  for (int bsel = 0; bsel < 2; ++bsel)
-    if (chunk_first + bsel <= chunk_last)
-      fill_u_tile<W, KS>(smem + L::B_OFF + bsel * KS * L::BBYTES, U, chunk_first + bsel, C, R);
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -190,20 +207,24 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first();
-      const uint64_t pol_keep = policy_evict_last();   // z is re-read for every chunk
+      const uint64_t pol_keep = policy_evict_last();   // z and U are re-read by many items
       int it = 0;
-      for (long long i = i0; i < i1; ++i, ++it) {
+      for (; it < nmine; ++it) {
         const int s = it % NST;
         const uint32_t ph = (it / NST) & 1;
         if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_tc_error, 1)) break;
-        const Item itm = decode(i, nbt, ntiles);
+        const Item itm = decode_tm(blockIdx.x + static_cast<long long>(it) * gridDim.x,
+                                   nchunks, ntiles);
         const uint32_t full = bar_full + 8 * s;
+        const uint32_t st = sb + s * L::STAGE;
         mbar_expect_tx(full, L::TX);
-        tma_load_3d(sb + L::X_OFF + s * L::XBYTES, &tm_x, full, itm.chunk * CC,
-                    itm.t0 - (W - 1), itm.b, pol_stream);
+        tma_load_3d(st, &tm_x, full, itm.chunk * CC, itm.t0 - (W - 1), itm.b, pol_stream);
         for (int ks = 0; ks < KS; ++ks)
-          tma_load_3d(sb + L::Z_OFF + (s * KS + ks) * L::ZBYTES, &tm_z, full, ks * 16, itm.t0,
-                      itm.b, pol_keep);
+          tma_load_3d(st + L::Z_IN + ks * L::ZBYTES, &tm_z, full, ks * 16, itm.t0, itm.b,
+                      pol_keep);
+        for (int a = 0; a < W; ++a)
+          tma_load_3d(st + L::U_IN + a * L::UATOM, &tm_u, full, itm.chunk * L::NCOL + a * 64, 0,
+                      0, pol_keep);
       }
       // Let every load this thread issued land before the CTA can exit.
       for (int j = std::max(0, it - NST); j < it; ++j)
@@ -212,9 +233,11 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, L::NCOL);
+      // A = z tile (K-major, 32-byte swizzle); B = the chunk's U columns in
+      // natural order (MN-major, 128-byte swizzle, 64-column atoms).
+      constexpr uint32_t idesc = idesc_major(BM, L::NCOL, 0, 1);
       int it = 0;
-      for (long long i = i0; i < i1; ++i, ++it) {
+      for (; it < nmine; ++it) {
         const int s = it % NST;
         const uint32_t ph = (it / NST) & 1;
         const int a = it & 1;
@@ -222,11 +245,11 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         if (!mbar_wait(bar_acce + 8 * a, aph ^ 1, abort_flag, &g_tc_error, 2)) break;
         if (!mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_tc_error, 2)) break;
         tc_fence_after();
-        const int bsel = static_cast<int>(i / nbt) - chunk_first;
+        const uint32_t st = sb + s * L::STAGE;
         const uint32_t d = tmem + a * 256;
         for (int ks = 0; ks < KS; ++ks) {
-          const uint64_t ad = desc_kmajor_sw32(sb + L::Z_OFF + (s * KS + ks) * L::ZBYTES);
-          const uint64_t bd = desc_kmajor_sw32(sb + L::B_OFF + (bsel * KS + ks) * L::BBYTES);
+          const uint64_t ad = desc_kmajor_sw32(st + L::Z_IN + ks * L::ZBYTES);
+          const uint64_t bd = make_desc(st + L::U_IN + ks * 2048, L::UATOM, 1024, 2);
           mma_bf16(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
         }
         mma_commit(bar_accf + 8 * a);
@@ -236,42 +259,43 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     }
   } else {
     // --------------------------------------------------------- epilogue --
+    // Two independent groups of 8 warps: group g takes the items it with
+    // it % 2 == g, using TMEM accumulator g and y staging buffer g, so one
+    // group's loads, math and store overlap the other group's.
+    const int g = (warp - 2) >> 3;
     const int lg = warp & 3;                 // TMEM lane group of this warp
-    const int h = (warp - 2) >> 2;           // channel half of the chunk
+    const int h = ((warp - 2) >> 2) & 1;     // channel half of the chunk
     const int tl = lg * 32 + lane;           // token within the tile
-    const bool storer = (warp == 2 && lane == 0);
+    const bool storer = ((warp - 2) & 7) == 0 && lane == 0;
     const uint64_t pol_y = policy_evict_first();
-    const uint32_t tbase = tmem + (static_cast<uint32_t>(lg * 32) << 16);
-    int it = 0;
-    for (long long i = i0; i < i1; ++i, ++it) {
+    const uint32_t tbase = tmem + (static_cast<uint32_t>(lg * 32) << 16) + g * 256;
+    const uint32_t ybuf = sb + L::Y_OFF + g * L::YBYTES;
+    for (int it = g; it < nmine; it += 2) {
       const int s = it % NST;
       const uint32_t ph = (it / NST) & 1;
-      const int a = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      const uint32_t ybuf = sb + L::Y_OFF + a * L::YBYTES;
       if (storer) {
-        bulk_wait_read<1>();                 // the store that used this buffer has read it
-        mbar_arrive(bar_yfree + 8 * a);
+        bulk_wait_read<0>();                 // this group's previous store has read the buffer
+        mbar_arrive(bar_yfree + 8 * g);
       }
       // Every lane waits; the warp leaves together if any wait gave up, so
       // the .sync.aligned TMEM loads below always run converged.
-      bool ok = mbar_wait(bar_yfree + 8 * a, aph, abort_flag, &g_tc_error, 3) &&
-                mbar_wait(bar_accf + 8 * a, aph, abort_flag, &g_tc_error, 3) &&
+      bool ok = mbar_wait(bar_yfree + 8 * g, aph, abort_flag, &g_tc_error, 3) &&
+                mbar_wait(bar_accf + 8 * g, aph, abort_flag, &g_tc_error, 3) &&
                 mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_tc_error, 3);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const uint32_t xt = sb + L::X_OFF + s * L::XBYTES;
+      const uint32_t xt = sb + s * L::STAGE;
+      // Four 8-channel chunks per warp; tap k of channel c is column c*W + k.
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int cch = 4 * h + q;           // 16-byte chunk of the 128-byte row
         uint32_t acc[8 * W];
-        tmem_ld_cols<8 * W>(tbase + a * 256 + (h * 32 + q * 8) * W, acc);
+        tmem_ld_cols<8 * W>(tbase + cch * 8 * W, acc);
         float xv[W][8];
 #pragma unroll
-        for (int k = 0; k < W; ++k) {
-          const uint32_t row = tl + (W - 1) - k;
-          unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(row, cch)), xv[k]);
-        }
+        for (int k = 0; k < W; ++k)
+          unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch)), xv[k]);
         tmem_wait_ld();
         tmem_regs_ready<8 * W>(acc);
         float out[8];
@@ -288,14 +312,15 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar_acce + 8 * a);
+        mbar_arrive(bar_acce + 8 * g);
         mbar_arrive(bar_empty + 8 * s);
-        mbar_arrive(bar_yfull + 8 * a);
+        mbar_arrive(bar_yfull + 8 * g);
       }
       // On a failed wait the store is skipped; the abort flag is up, so the
       // whole warp leaves at the next item's waits.
-      if (storer && mbar_wait(bar_yfull + 8 * a, aph, abort_flag, &g_tc_error, 4)) {
-        const Item itm = decode(i, nbt, ntiles);
+      if (storer && mbar_wait(bar_yfull + 8 * g, aph, abort_flag, &g_tc_error, 4)) {
+        const Item itm = decode_tm(blockIdx.x + static_cast<long long>(it) * gridDim.x,
+                                   nchunks, ntiles);
         tma_store_3d(&tm_y, ybuf, itm.chunk * CC, itm.t0, itm.b, pol_y);
         bulk_commit();
       }
@@ -338,10 +363,13 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 //
 // Roles: warp 0 producer (TMA boxes of x [t0-W+1, t0+128), dy [t0, t0+127+W)
 // and z [t0, t0+127+W), plus one 1-D bulk copy of the chunk's U tiles per
-// chunk), warp 1 TMEM owner and MMA issuer, warps 2-9 epilogue.  Per item
-// the epilogue (a) reads D_k and dy, writes dx (staged, TMA store) and frees
-// D so the MMA of the next item can start, (b) forms dw into the dw tiles;
-// at chunk ends it reads out the dU accumulator, at the end the dz ones.
+// chunk), warp 1 TMEM owner and issuer of the D_k MMAs, warp 18 issuer of
+// the dz and dU MMAs (two issuers, so the dx path never waits behind the dw
+// path), warps 2-9 the dx group (reads
+// D_k and dy, writes dx through a staged TMA store and frees D so the MMAs
+// of the next item can start), warps 10-17 the dw group (forms dw into the
+// dw tiles one tap pair at a time; at chunk ends it reads out the dU
+// accumulator, at the end the dz ones).  The two groups run independently.
 
 template <int W>
 struct BwdLayout {
@@ -361,9 +389,9 @@ struct BwdLayout {
   static constexpr int DW_OFF = U_OFF + 2 * UALLOC;
   static constexpr int DX_OFF = DW_OFF + NT * DWTAP;
   static constexpr int BAR_OFF = DX_OFF + BM * 128;
-  // full[3] empty[3] dfull dempty dwfull dwfree ufull[2] ufree[2] uafull[2]
-  // uaempty[2] dzfull yfull yfree
-  static constexpr int NBAR = 2 * NSTB + 4 + 8 + 3;
+  // full[3] empty[3] dfull dempty dwfull[2] dwfree[2] ufull[2] ufree[2]
+  // uafull[2] uaempty[2] dzfull yfull yfree
+  static constexpr int NBAR = 2 * NSTB + 2 + 4 + 8 + 3;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int TOTAL = MISC_OFF + 16 + 1024;
   static constexpr uint32_t TX = 2 * XBOX + ZBOX;
@@ -373,23 +401,8 @@ struct BwdLayout {
   static constexpr int TPS_MAX = (512 - TM_DZ) / 16;
 };
 
-// Shared-memory descriptors of the layouts above (fields as in sm100.cuh).
-// layout: 0 = no swizzle (8-row x 16-byte core matrices), 2 = 128-byte swizzle.
-__device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
-                                              uint32_t layout) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
-         (static_cast<uint64_t>(layout) << 61);
-}
-
-// kind::f16 instruction descriptor with operand majors (0 = K-major, 1 = MN-major).
-__host__ __device__ constexpr uint32_t idesc_major(uint32_t M, uint32_t N, uint32_t amaj,
-                                                   uint32_t bmaj) {
-  return idesc_bf16_f32(M, N) | (amaj << 15) | (bmaj << 16);
-}
-
 struct BwdArgs {
+  __nv_bfloat16* dx;       // [B][T][C]
   float* dz_part;          // [S][B*T][16]
   float* dU_part;          // [P][16][C*W]
   const unsigned char* uimg;  // [nchunks][W][16 rows][128 B] swizzled U tiles
@@ -397,7 +410,7 @@ struct BwdArgs {
 };
 
 template <int W>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
 lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
           const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dx,
           const BwdArgs args) {
@@ -423,9 +436,9 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   const uint32_t bar_empty = bar_full + NST_ * 8;
   const uint32_t bar_dfull = bar_empty + NST_ * 8;
   const uint32_t bar_dempty = bar_dfull + 8;
-  const uint32_t bar_dwfull = bar_dempty + 8;
-  const uint32_t bar_dwfree = bar_dwfull + 8;
-  const uint32_t bar_ufull = bar_dwfree + 8;
+  const uint32_t bar_dwfull = bar_dempty + 8;    // [2]: one per tap pair of the dw tiles
+  const uint32_t bar_dwfree = bar_dwfull + 16;   // [2]
+  const uint32_t bar_ufull = bar_dwfree + 16;
   const uint32_t bar_ufree = bar_ufull + 16;
   const uint32_t bar_uafull = bar_ufree + 16;
   const uint32_t bar_uaempty = bar_uafull + 16;
@@ -438,20 +451,22 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST_; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1 + NEPI);
+      mbar_init(bar_empty + 8 * s, 2 + 2 * NEPI);   // both MMA issuers, both groups
     }
     mbar_init(bar_dfull, 1);
     mbar_init(bar_dempty, NEPI);
-    mbar_init(bar_dwfull, NEPI);
-    mbar_init(bar_dwfree, 1);
+    for (int pr = 0; pr < 2; ++pr) {
+      mbar_init(bar_dwfull + 8 * pr, NEPI);
+      mbar_init(bar_dwfree + 8 * pr, 1);
+    }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_ufull + 8 * a, 1);
-      mbar_init(bar_ufree + 8 * a, 1);
+      mbar_init(bar_ufree + 8 * a, 2);                // both MMA issuers read U
       mbar_init(bar_uafull + 8 * a, 1);
       mbar_init(bar_uaempty + 8 * a, NEPI);
     }
     mbar_init(bar_dzfull, 1);
-    mbar_init(bar_yfull, NEPI);
+    mbar_init(bar_yfull, NEPI);     // (unused: dx is stored from registers)
     mbar_init(bar_yfree, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -517,222 +532,273 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         drain_wait(bar_ufull + 8 * (lc & 1), (lc >> 1) & 1);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer --
+    // --------------------------------------------------- D-MMA issuer --
+    // D_k for every item, as soon as the dx group has freed D.
     if (lane == 0) {
       constexpr uint32_t id_d = idesc_major(BM, 64, 0, 1);    // A z K-major, B U MN-major
+      const uint32_t zsbo = L::XROWS * 16;                    // stride of the two z halves
+      int n = 0;
+      for (; n < nitems; ++n) {
+        const int lc = n / ntile, lt = n - lc * ntile;
+        const int s = n % NST_;
+        bool ok = true;
+        if (lt == 0)
+          ok = mbar_wait(bar_ufull + 8 * (lc & 1), (lc >> 1) & 1, abort_flag, &g_tc_error, 2);
+        ok = ok && mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 2) &&
+             mbar_wait(bar_dempty, (n & 1) ^ 1, abort_flag, &g_tc_error, 2);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
+        const uint32_t ut = sb + L::U_OFF + (lc & 1) * L::UALLOC;
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+          mma_bf16(tmem + L::TM_D + k * 64, make_desc(zt + 16 * k, zsbo, 128, 0),
+                   make_desc(ut + k * 2048, 16, 1024, 2), id_d, 0u);
+        mma_commit(bar_dfull);
+        mma_commit(bar_empty + 8 * s);
+        if (lt == ntile - 1) mma_commit(bar_ufree + 8 * (lc & 1));
+      }
+      // Let every MMA this thread issued finish before TMEM is freed.
+      if (n > 0) drain_wait(bar_dfull, (n - 1) & 1);
+    }
+  } else if (warp == kDzduWarp) {
+    // ------------------------------------------------- dz/dU-MMA issuer --
+    // dz and dU for every item, one tap pair at a time as the dw group
+    // finishes writing it.
+    if (lane == 0) {
       constexpr uint32_t id_dz = idesc_major(BM, 16, 0, 0);   // A dw K-major, B U K-major
       constexpr uint32_t id_du = idesc_major(BM, 16, 1, 1);   // A dw^T MN-major, B z MN-major
-      const uint32_t zsbo = L::XROWS * 16;                    // stride of the two z halves
+      const uint32_t zsbo = L::XROWS * 16;
       bool ok = true;
-      int issued_d = 0, issued_dzdu = 0;
-      for (int n = 0; n <= nitems && ok; ++n) {
-        if (n < nitems) {
-          // ---- D_k for item n
-          const int lc = n / ntile, lt = n - lc * ntile;
-          const int s = n % NST_;
-          if (lt == 0)
-            ok = ok && mbar_wait(bar_ufull + 8 * (lc & 1), (lc >> 1) & 1, abort_flag,
-                                 &g_tc_error, 2);
-          ok = ok && mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 2);
-          ok = ok && mbar_wait(bar_dempty, (n & 1) ^ 1, abort_flag, &g_tc_error, 2);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
-          const uint32_t ut = sb + L::U_OFF + (lc & 1) * L::UALLOC;
-#pragma unroll
-          for (int k = 0; k < W; ++k)
-            mma_bf16(tmem + L::TM_D + k * 64, make_desc(zt + 16 * k, zsbo, 128, 0),
-                     make_desc(ut + k * 2048, 16, 1024, 2), id_d, 0u);
-          mma_commit(bar_dfull);
-          ++issued_d;
-        }
-        if (n > 0) {
-          // ---- dz and dU for item m = n - 1
-          const int m = n - 1;
-          const int lc = m / ntile, lt = m - lc * ntile;
-          const int s = m % NST_;
-          const int ub = lc & 1;
-          ok = ok && mbar_wait(bar_dwfull, m & 1, abort_flag, &g_tc_error, 2);
-          if (lt == 0 && lc >= 2)
+      int issued_pair[2] = {0, 0};
+      for (int m = 0; m < nitems && ok; ++m) {
+        const int lc = m / ntile, lt = m - lc * ntile;
+        const int s = m % NST_;
+        const int ub = lc & 1;
+        if (lt == 0) {
+          ok = mbar_wait(bar_ufull + 8 * ub, (lc >> 1) & 1, abort_flag, &g_tc_error, 5);
+          if (lc >= 2)
             ok = ok && mbar_wait(bar_uaempty + 8 * ub, ((lc >> 1) & 1) ^ 1, abort_flag,
-                                 &g_tc_error, 2);
+                                 &g_tc_error, 5);
+        }
+        ok = ok && mbar_wait(bar_full + 8 * s, (m / NST_) & 1, abort_flag, &g_tc_error, 5);
+        if (!ok) break;
+        const uint32_t dw = sb + L::DW_OFF;
+        const uint32_t ut = sb + L::U_OFF + ub * L::UALLOC;
+        const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
+#pragma unroll
+        for (int pr = 0; pr < L::NT / 2; ++pr) {
+          ok = mbar_wait(bar_dwfull + 8 * pr, m & 1, abort_flag, &g_tc_error, 5);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t dw = sb + L::DW_OFF;
-          const uint32_t ut = sb + L::U_OFF + ub * L::UALLOC;
-          const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
-          // dz[t, :] (+)= sum over the chunk's 64*W columns (tap-major)
+          // Two accumulation chains, interleaved so that consecutive MMAs
+          // never feed each other:
+          //   dz[t, :]   (+)= the pair's 128 columns (tap-major, 16 per K-step)
+          //   dU^T[j', :](+)= the tile's 128 tokens; M block pr = taps 2pr, 2pr+1
 #pragma unroll
-          for (int q = 0; q < 4 * W; ++q) {
+          for (int i = 0; i < 8; ++i) {
+            const int q = 8 * pr + i;
             const int k = q >> 2, cb = q & 3;
-            mma_bf16(tmem + L::TM_DZ + lt * 16,
-                     make_desc(dw + k * L::DWTAP + cb * 32, 16, 1024, 2),
-                     make_desc(ut + k * 2048 + cb * 32, 16, 1024, 2), id_dz,
-                     (lc > 0 || q > 0) ? 1u : 0u);
+            if (k < W)
+              mma_bf16(tmem + L::TM_DZ + lt * 16,
+                       make_desc(dw + k * L::DWTAP + cb * 32, 16, 1024, 2),
+                       make_desc(ut + k * 2048 + cb * 32, 16, 1024, 2), id_dz,
+                       (lc > 0 || q > 0) ? 1u : 0u);
+            mma_bf16(tmem + L::TM_DU + ub * (L::NT / 2) * 16 + pr * 16,
+                     make_desc(dw + 2 * pr * L::DWTAP + i * 2048, L::DWTAP, 1024, 2),
+                     make_desc(zt + i * 256, 128, zsbo, 0), id_du,
+                     (lt > 0 || i > 0) ? 1u : 0u);
           }
-          // dU^T[j', :] (+)= over the tile's 128 tokens; M block mb = taps 2mb, 2mb+1
-#pragma unroll
-          for (int mb = 0; mb < L::NT / 2; ++mb)
-#pragma unroll
-            for (int ks = 0; ks < BM / 16; ++ks)
-              mma_bf16(tmem + L::TM_DU + ub * (L::NT / 2) * 16 + mb * 16,
-                       make_desc(dw + 2 * mb * L::DWTAP + ks * 2048, L::DWTAP, 1024, 2),
-                       make_desc(zt + ks * 256, 128, zsbo, 0), id_du,
-                       (lt > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar_dwfree);
-          mma_commit(bar_empty + 8 * s);
-          if (lt == ntile - 1) {
-            mma_commit(bar_uafull + 8 * ub);
-            mma_commit(bar_ufree + 8 * ub);
-          }
-          ++issued_dzdu;
+          mma_commit(bar_dwfree + 8 * pr);
+          ++issued_pair[pr];
+        }
+        if (!ok) break;
+        mma_commit(bar_empty + 8 * s);
+        if (lt == ntile - 1) {
+          mma_commit(bar_uafull + 8 * ub);
+          mma_commit(bar_ufree + 8 * ub);
         }
       }
       if (ok && nitems > 0) mma_commit(bar_dzfull);
       // Let every MMA this thread issued finish before TMEM is freed.
-      if (issued_dzdu > 0) drain_wait(bar_dwfree, (issued_dzdu - 1) & 1);
-      if (issued_d > 0) drain_wait(bar_dfull, (issued_d - 1) & 1);
+      for (int pr = 0; pr < 2; ++pr)
+        if (issued_pair[pr] > 0) drain_wait(bar_dwfree + 8 * pr, (issued_pair[pr] - 1) & 1);
     }
   } else {
-    // --------------------------------------------------------- epilogue --
+    // ---------------------------------------------------------- epilogues --
+    // Two groups of 8 warps that run independently, item by item:
+    //   warps 2-9   (dx group): dx = res*dy + sum_k D_k dy[t+k], staged and
+    //               stored with TMA; frees D for the next item's MMAs.
+    //   warps 10-17 (dw group): dw tiles, one tap pair at a time; the dU
+    //               readout at chunk ends and the dz readout at the end.
+    // In each group warp (w % 4) owns TMEM lanes 32*(w % 4) .. +31 (tokens)
+    // and the two warps of a lane group split the chunk's channels.
+    const bool dx_group = warp < 2 + NEPI;
     const int lg = warp & 3;
-    const int h = (warp - 2) >> 2;
+    const int h = ((warp - 2) >> 2) & 1;
     const int tl = lg * 32 + lane;
-    const bool storer = (warp == 2 && lane == 0);
-    const uint64_t pol_y = policy_evict_first();
     const uint32_t tlane = static_cast<uint32_t>(lg * 32) << 16;
-    const uint32_t dxs = sb + L::DX_OFF;
     bool ok = true;
-    for (int n = 0; n < nitems; ++n) {
-      const int lc = n / ntile, lt = n - lc * ntile;
-      const int s = n % NST_;
-      const int gt = tl0 + lt;
-      const int b = gt / args.ntiles, t0 = (gt - b * args.ntiles) * BM;
-      const int c0 = (ch0 + lc) * CC;
-      const uint32_t st = sb + L::STG_OFF + s * L::STAGE;
-      const uint32_t xt = st, dyt = st + L::XBYTES;
-      if (storer) {
-        bulk_wait_read<0>();
-        mbar_arrive(bar_yfree);
-      }
-      ok = mbar_wait(bar_yfree, n & 1, abort_flag, &g_tc_error, 3) &&
-           mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3) &&
-           mbar_wait(bar_dfull, n & 1, abort_flag, &g_tc_error, 3);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      // (a) dx from D_k and dy; keep dy[t] for (b)
-      uint4 dyk[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int cch = 4 * h + q;
-        uint32_t dk[W][8];
-#pragma unroll
-        for (int k = 0; k < W; ++k) tmem_ld8(tmem + tlane + L::TM_D + k * 64 + 32 * h + 8 * q, dk[k]);
-        float g[W][8];
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          const uint4 raw = lds128(dyt + sw128_offset(tl + k, cch));
-          if (k == 0) dyk[q] = raw;
-          unpack16<__nv_bfloat16>(raw, g[k]);
-        }
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < W; ++k) tmem_regs_ready<8>(dk[k]);
-        float out[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float v = args.residual ? g[0][c] : 0.f;
-#pragma unroll
-          for (int k = 0; k < W; ++k) v = fmaf(__uint_as_float(dk[k][c]), g[k][c], v);
-          out[c] = v;
-        }
-        sts128(dxs + sw128_offset(tl, cch), pack16<__nv_bfloat16>(out));
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar_dempty);
-        mbar_arrive(bar_yfull);
-      }
-      if (storer && mbar_wait(bar_yfull, n & 1, abort_flag, &g_tc_error, 4)) {
-        tma_store_3d(&tm_dx, dxs, c0, t0, b, pol_y);
-        bulk_commit();
-      }
-      // (b) dw[t,c,k] = dy[t,c] x[t-k,c] into the tap tiles
-      ok = mbar_wait(bar_dwfree, (n & 1) ^ 1, abort_flag, &g_tc_error, 3);
-      if (!__all_sync(0xffffffffu, ok)) break;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int cch = 4 * h + q;
-        float g[8];
-        unpack16<__nv_bfloat16>(dyk[q], g);
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          float xv[8], p[8];
-          unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch)), xv);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) p[c] = g[c] * xv[c];
-          sts128(sb + L::DW_OFF + k * L::DWTAP + sw128_offset(tl, cch),
-                 pack16<__nv_bfloat16>(p));
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar_dwfull);
-        mbar_arrive(bar_empty + 8 * s);
-      }
-      // (c) end of a chunk: read out its dU^T accumulator
-      if (lt == ntile - 1) {
-        const int ub = lc & 1;
-        ok = mbar_wait(bar_uafull + 8 * ub, (lc >> 1) & 1, abort_flag, &g_tc_error, 3);
+    if (dx_group) {
+      // dx[t] = res*dy[t] + sum_k D_k[t] dy[t+k]: each thread reads its own
+      // dy row; rows t+1..t+3 come from the neighbouring lanes, and only the
+      // last k lanes of a warp read row t+k from shared memory.  dx goes
+      // straight from registers to global memory.
+      for (int n = 0; n < nitems; ++n) {
+        const int lc = n / ntile, lt = n - lc * ntile;
+        const int s = n % NST_;
+        const int gt = tl0 + lt;
+        const int b = gt / args.ntiles, t0 = (gt - b * args.ntiles) * BM;
+        const int c0 = (ch0 + lc) * CC;
+        const uint32_t dyt = sb + L::STG_OFF + s * L::STAGE + L::XBYTES;
+        ok = mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3) &&
+             mbar_wait(bar_dfull, n & 1, abort_flag, &g_tc_error, 3);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
-        if (h < L::NT / 2) {
-          uint32_t v[16];
-          tmem_ld16(tmem + tlane + L::TM_DU + ub * (L::NT / 2) * 16 + h * 16, v);
-          tmem_wait_ld();
-          tmem_regs_ready<16>(v);
-          const int jp = h * 128 + tl;                    // tap-major column of the chunk
-          const int k = jp >> 6, c = c0 + (jp & 63);
-          if (k < W && c < args.C) {
-            float* dst = args.dU_part + static_cast<size_t>(split) * 16 * CW +
-                         static_cast<int64_t>(c) * W + k;
+        const bool row_ok = t0 + tl < args.T;
+        __nv_bfloat16* dxrow = args.dx + (static_cast<int64_t>(b) * args.T + t0 + tl) * args.C + c0;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) dst[static_cast<int64_t>(r) * CW] = __uint_as_float(v[r]);
+        for (int q = 0; q < 4; ++q) {
+          const int cch = 4 * h + q;
+          uint32_t dk[W][8];
+#pragma unroll
+          for (int k = 0; k < W; ++k)
+            tmem_ld8(tmem + tlane + L::TM_D + k * 64 + 32 * h + 8 * q, dk[k]);
+          uint4 gr[W];
+          gr[0] = lds128(dyt + sw128_offset(tl, cch));
+#pragma unroll
+          for (int k = 1; k < W; ++k) {
+            gr[k].x = __shfl_down_sync(0xffffffffu, gr[0].x, k);
+            gr[k].y = __shfl_down_sync(0xffffffffu, gr[0].y, k);
+            gr[k].z = __shfl_down_sync(0xffffffffu, gr[0].z, k);
+            gr[k].w = __shfl_down_sync(0xffffffffu, gr[0].w, k);
+            if (lane >= 32 - k) gr[k] = lds128(dyt + sw128_offset(tl + k, cch));
           }
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < W; ++k) tmem_regs_ready<8>(dk[k]);
+          float2 o[4];
+          const uint32_t g0[4] = {gr[0].x, gr[0].y, gr[0].z, gr[0].w};
+#pragma unroll
+          for (int p = 0; p < 4; ++p) o[p] = args.residual ? bf2f(g0[p]) : make_float2(0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            const uint32_t gw[4] = {gr[k].x, gr[k].y, gr[k].z, gr[k].w};
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+              o[p] = __ffma2_rn(f2(dk[k][2 * p], dk[k][2 * p + 1]), bf2f(gw[p]), o[p]);
+          }
+          if (row_ok && c0 + 8 * cch < args.C)
+            stcs16(dxrow + 8 * cch, make_uint4(f2bf(o[0]), f2bf(o[1]), f2bf(o[2]), f2bf(o[3])));
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_uaempty + 8 * ub);
+        if (lane == 0) {
+          mbar_arrive(bar_dempty);
+          mbar_arrive(bar_empty + 8 * s);
+        }
       }
-    }
-    // (d) the dz accumulators of every tile of the split
-    if (ok && nitems > 0) {
-      ok = mbar_wait(bar_dzfull, 0, abort_flag, &g_tc_error, 3);
-      if (__all_sync(0xffffffffu, ok)) {
-        tc_fence_after();
-        for (int lt = h; lt < ntile; lt += 2) {
-          uint32_t v[16];
-          tmem_ld16(tmem + tlane + L::TM_DZ + lt * 16, v);
-          tmem_wait_ld();
-          tmem_regs_ready<16>(v);
-          const int gt = tl0 + lt;
-          const int b = gt / args.ntiles, t = (gt - b * args.ntiles) * BM + tl;
-          if (t < args.T) {
-            float4* dst = reinterpret_cast<float4*>(
-                args.dz_part + (static_cast<size_t>(slice) * Ntok +
-                                static_cast<int64_t>(b) * args.T + t) * 16);
+    } else {
+      // dw[t,c,k] = dy[t,c] x[t-k,c].  Thread (chunk wc of 8 channels, run of
+      // 4 tokens) keeps a window of x rows in registers, so each x and dy row
+      // is read once.  The product of two bf16 is exact in fp32, so one
+      // bf16x2 multiply (round to nearest) gives the same bf16 as the fp32
+      // product rounded once.
+      const int wt = threadIdx.x - (2 + NEPI) * 32;     // 0..255 in the dw group
+      const int wc = wt & 7;                            // 16-byte chunk of the row
+      const int r0 = (wt >> 3) * 4;                     // first token of the run
+      for (int n = 0; n < nitems; ++n) {
+        const int lc = n / ntile, lt = n - lc * ntile;
+        const int s = n % NST_;
+        const int c0 = (ch0 + lc) * CC;
+        const uint32_t xt = sb + L::STG_OFF + s * L::STAGE, dyt = xt + L::XBYTES;
+        ok = mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        // x box row r holds token t0 - (W-1) + r; token r0 + i needs rows
+        // r0 + i + (W-1) - k.
+        uint4 xw[4 + W - 1];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        for (int j = 0; j < 4 + W - 1; ++j) xw[j] = lds128(xt + sw128_offset(r0 + j, wc));
+        uint4 gw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) gw[i] = lds128(dyt + sw128_offset(r0 + i, wc));
+#pragma unroll
+        for (int pr = 0; pr < L::NT / 2; ++pr) {
+          ok = mbar_wait(bar_dwfree + 8 * pr, (n & 1) ^ 1, abort_flag, &g_tc_error, 3);
+          if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+          for (int k = 2 * pr; k < 2 * pr + 2; ++k) {
+            if (k < W) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gw[i]);
+                const __nv_bfloat162* x2 =
+                    reinterpret_cast<const __nv_bfloat162*>(&xw[i + (W - 1) - k]);
+                __nv_bfloat162 p2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) p2[e] = __hmul2(g2[e], x2[e]);
+                sts128(sb + L::DW_OFF + k * L::DWTAP + sw128_offset(r0 + i, wc),
+                       *reinterpret_cast<const uint4*>(p2));
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dwfull + 8 * pr);
+        }
+        if (!ok) break;
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        // End of a chunk: read out its dU^T accumulator (TMEM lanes = columns).
+        if (lt == ntile - 1) {
+          const int ub = lc & 1;
+          ok = mbar_wait(bar_uafull + 8 * ub, (lc >> 1) & 1, abort_flag, &g_tc_error, 3);
+          if (!__all_sync(0xffffffffu, ok)) break;
+          tc_fence_after();
+          if (h < L::NT / 2) {
+            uint32_t v[16];
+            tmem_ld16(tmem + tlane + L::TM_DU + ub * (L::NT / 2) * 16 + h * 16, v);
+            tmem_wait_ld();
+            tmem_regs_ready<16>(v);
+            const int jp = h * 128 + tl;                  // tap-major column of the chunk
+            const int k = jp >> 6, c = c0 + (jp & 63);
+            if (k < W && c < args.C) {
+              float* dst = args.dU_part + static_cast<size_t>(split) * 16 * CW +
+                           static_cast<int64_t>(c) * W + k;
+#pragma unroll
+              for (int r = 0; r < 16; ++r)
+                dst[static_cast<int64_t>(r) * CW] = __uint_as_float(v[r]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_uaempty + 8 * ub);
+        }
+      }
+      // The dz accumulators of every tile of the split.
+      if (ok && nitems > 0) {
+        ok = mbar_wait(bar_dzfull, 0, abort_flag, &g_tc_error, 3);
+        if (__all_sync(0xffffffffu, ok)) {
+          tc_fence_after();
+          for (int lt = h; lt < ntile; lt += 2) {
+            uint32_t v[16];
+            tmem_ld16(tmem + tlane + L::TM_DZ + lt * 16, v);
+            tmem_wait_ld();
+            tmem_regs_ready<16>(v);
+            const int gt = tl0 + lt;
+            const int b = gt / args.ntiles, t = (gt - b * args.ntiles) * BM + tl;
+            if (t < args.T) {
+              float4* dst = reinterpret_cast<float4*>(
+                  args.dz_part + (static_cast<size_t>(slice) * Ntok +
+                                  static_cast<int64_t>(b) * args.T + t) * 16);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            }
           }
         }
       }
     }
-    if (storer) bulk_wait<0>();
   }
 
   tc_fence_before();
@@ -840,9 +906,10 @@ template <int W, int KS>
 cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, const Shape& s,
                        cudaStream_t st) {
   using L = FwdLayout<W, KS>;
-  CUtensorMap tx, tz, ty;
+  CUtensorMap tx, tz, tu, ty;
   if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, BM + W - 1, 128) ||
       !make_tmap_3d(&tz, z, true, s.R, s.T, s.B, 16, BM, 32) ||
+      !make_tmap_3d(&tu, U, true, s.C * s.W, s.R, 1, 64, 16 * KS, 128) ||
       !make_tmap_3d(&ty, y, true, s.C, s.T, s.B, CC, BM, 128))
     return cudaErrorInvalidValue;
   const int ntiles = static_cast<int>((s.T + BM - 1) / BM);
@@ -851,14 +918,12 @@ cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, con
   const long long items = nbt * nchunks;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
-  long long grid = std::min<long long>(sms, items);
-  grid = std::max<long long>(grid, nchunks);
+  const long long grid = std::min<long long>(sms, items);
   auto kern = lr_fwd_tc<W, KS>;
   cudaError_t e = set_smem<L>(kern, L::TOTAL);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kFwdThreads, L::TOTAL, st>>>(
-      tx, tz, ty, static_cast<const __nv_bfloat16*>(U), static_cast<int>(s.C),
-      static_cast<int>(s.R), ntiles, static_cast<int>(nbt), nchunks, s.residual);
+      tx, tz, tu, ty, ntiles, static_cast<int>(nbt), nchunks, s.residual);
   return cudaGetLastError();
 }
 
@@ -930,6 +995,7 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
     return cudaErrorInvalidValue;
   unsigned char* base = static_cast<unsigned char*>(ws);
   BwdArgs a;
+  a.dx = static_cast<__nv_bfloat16*>(dx);
   a.dz_part = reinterpret_cast<float*>(base + p.dz_off);
   a.dU_part = reinterpret_cast<float*>(base + p.dU_off);
   a.uimg = base + p.img_off;
@@ -952,7 +1018,7 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
   auto kern = lr_bwd_tc<W>;
   cudaError_t e = set_smem<L>(kern, L::TOTAL);
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(p.S * p.P), kFwdThreads, L::TOTAL, st>>>(tx, tdy, tz, tdx, a);
+  kern<<<static_cast<unsigned>(p.S * p.P), kBwdThreads, L::TOTAL, st>>>(tx, tdy, tz, tdx, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t nz4 = s.B * s.T * 16 / 4, nU4 = 16 * s.C * s.W / 4;
