@@ -41,8 +41,8 @@ METRIC = "DSC fwd+bwd achieved HBM GB/s (% of B300 peak) and Mtokens/s at C=6144
 WORKLOAD = ("DSC at C=6144 W=4, B=8 T=2048 (16384 tokens), bf16, residual: head-wise "
             "H=16 fwd+bwd and low-rank R=16 H=1 fwd+bwd")
 KERNEL_SOURCES = {
-    "headwise_fwd": "lm_local_sequence_causal_b300/csrc/headwise.cu",
-    "headwise_bwd": "lm_local_sequence_causal_b300/csrc/headwise.cu",
+    "headwise_fwd": "lm_local_sequence_causal_b300/csrc/headwise_tma.cu",
+    "headwise_bwd": "lm_local_sequence_causal_b300/csrc/headwise_tma.cu",
     "lowrank_fwd": "lm_local_sequence_causal_b300/csrc/lowrank_tc.cu",
     "lowrank_bwd": "lm_local_sequence_causal_b300/csrc/lowrank_tc.cu",
 }

@@ -146,8 +146,17 @@ int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H,
                                   int64_t W, int64_t R, dsc_dtype_t dtype);
 
 /*
- * Diagnostic: the device error word of the tensor-core kernels on the
- * current device.  0 means no error; otherwise it holds the code of the
+ * 1 if dsc_headwise_fwd / dsc_headwise_bwd run these arguments on the
+ * TMA-staged kernels (bf16, C % 64 == 0, (H, W) in {(8, any W), (16, 2),
+ * (16, 4), (32, 4)}), 0 if on the register-streaming ones, -1 if the
+ * arguments are invalid.  Host only; touches no device.
+ */
+int dsc_headwise_uses_tma(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
+                          dsc_dtype_t dtype);
+
+/*
+ * Diagnostic: the device error word of the tensor-core and TMA kernels on
+ * the current device.  0 means no error; otherwise it holds the code of the
  * first bounded wait that gave up (1 producer, 2 MMA issuer, 3 epilogue,
  * 4 store, 5 second MMA issuer), after which that kernel returned early and
  * its outputs are

@@ -154,7 +154,17 @@ int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H, in
 
 dsc_status_t dsc_device_error(unsigned int* code, int reset) {
   if (code == nullptr) return DSC_ERR_INVALID_ARG;
-  return from_cuda(dsc::lowrank_tc_error(code, reset != 0));
+  unsigned int a = 0, b = 0;
+  cudaError_t e = dsc::lowrank_tc_error(&a, reset != 0);
+  if (e == cudaSuccess) e = dsc::headwise_tma_error(&b, reset != 0);
+  *code = a != 0 ? a : b;
+  return from_cuda(e);
+}
+
+int dsc_headwise_uses_tma(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
+                          dsc_dtype_t dtype) {
+  if (check_shape(B, T, C, H, W, 0, dtype, false) != DSC_OK) return -1;
+  return dsc::headwise_tma_supported(make_shape(B, T, C, H, W, 0, 0, dtype)) ? 1 : 0;
 }
 
 }  // extern "C"

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace dsc {
 
 struct Shape {
@@ -22,6 +24,15 @@ cudaError_t headwise_fwd(const void* x, const void* w, void* y, const Shape& s,
                          cudaStream_t st);
 cudaError_t headwise_bwd(const void* x, const void* w, const void* dy, void* dx,
                          void* dw, const Shape& s, cudaStream_t st);
+
+// Head-wise kernels with TMA-staged tiles (headwise_tma.cu): bf16, C % 64
+// == 0 and (H, W) in {(8, any), (16, 2), (16, 4), (32, 4)}.
+bool headwise_tma_supported(const Shape& s);
+cudaError_t headwise_fwd_tma(const void* x, const void* w, void* y, const Shape& s,
+                             cudaStream_t st);
+cudaError_t headwise_bwd_tma(const void* x, const void* w, const void* dy, void* dx, void* dw,
+                             const Shape& s, cudaStream_t st);
+cudaError_t headwise_tma_error(unsigned int* out, bool reset);
 
 // Low-rank kernels (lowrank_simt.cu).
 bool lowrank_supported(const Shape& s);
@@ -57,5 +68,26 @@ bool make_tmap_3d(CUtensorMap* tm, const void* base, bool bf16, uint64_t d0, uin
 bool make_tmap_4d_bf16(CUtensorMap* tm, const void* base, const uint64_t dims[4],
                        const uint64_t strides_bytes[3], const uint32_t box[4]);
 int sm_count();
+
+// Opt in to large dynamic shared memory, once per kernel and device.  The
+// template parameter `Tag` keeps one record per kernel instance (all
+// instances share a function type, so the type alone cannot tell them apart).
+template <typename Tag, typename F>
+cudaError_t set_smem(F* kernel, int bytes) {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
 
 }  // namespace dsc

@@ -1,0 +1,363 @@
+// headwise_tma.cu -- head-wise Dynamic Short Convolution, forward and backward,
+// with TMA-staged tiles (bf16, H in {8, 16, 32}).
+//
+// y[b,t,c] = res*x[b,t,c] + sum_{k<W} w[b,t,c/H,k] * x[b,t-k,c]   (x = 0 before t = 0)
+// ("Technische Samenvatting: Dynamische Korte Convoluties Verbeteren
+// Transformers", Methodologie: Mechanisme, Parametrisatie item 2, Plaatsing.)
+// Backward (chain rule of that definition):
+//   dx[b,s,c]   = res*dy[b,s,c] + sum_{k: s+k<T} w[b,s+k,c/H,k] dy[b,s+k,c]
+//   dw[b,t,g,k] = sum_{c in group g} dy[b,t,c] x[b,t-k,c]
+//
+// Pure streams over HBM.  A work item is (b, 128-token tile, 64-channel
+// chunk); one persistent CTA per SM takes items round-robin in tile-major
+// order, so neighbouring CTAs read neighbouring pieces of the same rows.
+//   warp 0      TMA producer, 4-stage ring: x rows [t0-W+1, t0+128) (the
+//               rows before t = 0 read as zero: the causal padding), in the
+//               backward also dy rows and w rows [t0, t0+127+W) (rows past T
+//               read as zero, which drops the terms with s+k >= T), and the
+//               w rows of the tile: the chunk's 64/H groups x W taps.
+//   warps 1-16  two independent groups of 8 warps that take alternate items,
+//               each with its own staged output tiles; in a group the warp
+//               (lane group lg = w % 4, half h) owns tokens 32*lg .. +31 and
+//               channels 32*h .. +31 of the chunk (four 8-channel pieces,
+//               which are whole groups since H >= 8).  Outputs go to staged
+//               tiles that one thread of the group stores with TMA.
+// Every mbarrier wait is bounded (sm100.cuh); a timeout records a code in
+// this file's device error word and the CTA returns.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "dsc_common.cuh"
+#include "dsc_internal.h"
+#include "sm100.cuh"
+
+namespace dsc {
+namespace {
+
+using namespace sm100;
+
+// Set when a bounded wait gives up: 1 = producer, 3 = epilogue, 4 = store.
+__device__ unsigned int g_hw_error = 0;
+
+constexpr int BM = 128;      // tokens per tile
+constexpr int CC = 64;       // channels per chunk (one 128-byte swizzled row)
+constexpr int NST = 4;       // input pipeline stages
+constexpr int NGRP = 8;      // warps per epilogue group
+constexpr int kThreads = (1 + 2 * NGRP) * 32;
+
+__host__ __device__ constexpr int round1k(int b) { return (b + 1023) / 1024 * 1024; }
+
+// Shared-memory layout of one configuration.  BWD adds the dy box and a
+// longer w box (the dx terms need w[s+k]) and the staged dw tile.
+template <int W, int H, bool BWD>
+struct HwLayout {
+  static constexpr int GI = CC / H;                  // groups per chunk
+  static constexpr int WROW = GI * W * 2;            // bytes of one token's taps
+  static constexpr int WSW = (WROW == 32 || WROW == 64) ? WROW : 0;  // swizzle of the w box
+  static constexpr int XROWS = BM + W - 1;
+  static constexpr int XBOX = XROWS * 128;
+  static constexpr int XBYTES = round1k(XBOX);
+  static constexpr int WROWS = BWD ? XROWS : BM;
+  static constexpr int WBOX = WROWS * WROW;
+  static constexpr int WBYTES = round1k(WBOX);
+  static constexpr int DY_IN = XBYTES;               // offsets inside a stage
+  static constexpr int W_IN = BWD ? 2 * XBYTES : XBYTES;
+  static constexpr int STAGE = W_IN + WBYTES;
+  static constexpr int OBYTES = BM * 128;            // staged y / dx tile of one group
+  static constexpr int DWBYTES = BWD ? round1k(BM * WROW) : 0;  // staged dw tile of one group
+  static constexpr int O_OFF = NST * STAGE;
+  static constexpr int DW_OFF = O_OFF + 2 * OBYTES;
+  static constexpr int BAR_OFF = DW_OFF + 2 * DWBYTES;
+  // full[NST] empty[NST] ofull[2] ofree[2]
+  static constexpr int NBAR = 2 * NST + 4;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int TOTAL = MISC_OFF + 16 + 1024;
+  static constexpr uint32_t TX = (BWD ? 2 : 1) * XBOX + WBOX;
+};
+
+// Byte offset of byte `o` of row `r` in a w tile of `row` bytes per row
+// stored by TMA with a `sw`-byte swizzle (0, 32 or 64).
+template <int row, int sw>
+__device__ __forceinline__ uint32_t wtile_offset(uint32_t r, uint32_t o) {
+  const uint32_t a = r * row + o;
+  if constexpr (sw == 32) return a ^ ((a >> 3) & 0x10u);
+  if constexpr (sw == 64) return a ^ ((a >> 3) & 0x30u);
+  return a;
+}
+
+__device__ __forceinline__ float lds_bf16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return __uint_as_float(static_cast<uint32_t>(v) << 16);
+}
+
+__device__ __forceinline__ void sts_bf16(uint32_t addr, float f) {
+  const unsigned short v = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+struct HwItem {
+  int chunk, b, t0;
+};
+__device__ __forceinline__ HwItem hw_decode(long long i, int nchunks, int ntiles) {
+  HwItem it;
+  const long long tile = i / nchunks;
+  it.chunk = static_cast<int>(i - tile * nchunks);
+  it.b = static_cast<int>(tile / ntiles);
+  it.t0 = static_cast<int>(tile - static_cast<long long>(it.b) * ntiles) * BM;
+  return it;
+}
+
+template <int W, int H, bool BWD>
+__global__ void __launch_bounds__(kThreads, 1)
+hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+              const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_out,
+              const __grid_constant__ CUtensorMap tm_dw, int ntiles, int nbt, int nchunks,
+              int residual) {
+  using L = HwLayout<W, H, BWD>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = align1k(smem_raw);
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long items = static_cast<long long>(nchunks) * nbt;
+  const int nmine = items > blockIdx.x
+                        ? static_cast<int>((items - 1 - blockIdx.x) / gridDim.x) + 1
+                        : 0;
+  const uint32_t bar_full = sb + L::BAR_OFF;
+  const uint32_t bar_empty = bar_full + NST * 8;
+  const uint32_t bar_ofull = bar_empty + NST * 8;
+  const uint32_t bar_ofree = bar_ofull + 16;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, NGRP);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(bar_ofull + 8 * g, NGRP);
+      mbar_init(bar_ofree + 8 * g, 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_out);
+    if constexpr (BWD) {
+      tma_prefetch_desc(&tm_dy);
+      tma_prefetch_desc(&tm_dw);
+    }
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer --
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int it = 0;
+      for (; it < nmine; ++it) {
+        const int s = it % NST;
+        if (!mbar_wait(bar_empty + 8 * s, ((it / NST) & 1) ^ 1, abort_flag, &g_hw_error, 1))
+          break;
+        const HwItem itm =
+            hw_decode(blockIdx.x + static_cast<long long>(it) * gridDim.x, nchunks, ntiles);
+        const uint32_t full = bar_full + 8 * s;
+        const uint32_t st = sb + s * L::STAGE;
+        mbar_expect_tx(full, L::TX);
+        tma_load_3d(st, &tm_x, full, itm.chunk * CC, itm.t0 - (W - 1), itm.b, pol);
+        if constexpr (BWD) tma_load_3d(st + L::DY_IN, &tm_dy, full, itm.chunk * CC, itm.t0, itm.b, pol);
+        tma_load_3d(st + L::W_IN, &tm_w, full, itm.chunk * L::GI * W, itm.t0, itm.b, pol);
+      }
+      for (int j = std::max(0, it - NST); j < it; ++j)
+        drain_wait(bar_full + 8 * (j % NST), (j / NST) & 1);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue --
+    const int g = (warp - 1) >> 3;             // group: items it with it % 2 == g
+    const int lg = warp & 3;
+    const int h = ((warp - 1) >> 2) & 1;
+    const int tl = lg * 32 + lane;
+    const bool storer = ((warp - 1) & 7) == 0 && lane == 0;
+    const uint64_t pol = policy_evict_first();
+    const uint32_t obuf = sb + L::O_OFF + g * L::OBYTES;
+    const uint32_t dwbuf = sb + L::DW_OFF + g * L::DWBYTES;
+    for (int it = g; it < nmine; it += 2) {
+      const int s = it % NST;
+      const uint32_t aph = (it >> 1) & 1;
+      if (storer) {
+        bulk_wait_read<0>();                   // this group's previous stores have read
+        mbar_arrive(bar_ofree + 8 * g);
+      }
+      bool ok = mbar_wait(bar_ofree + 8 * g, aph, abort_flag, &g_hw_error, 3) &&
+                mbar_wait(bar_full + 8 * s, (it / NST) & 1, abort_flag, &g_hw_error, 3);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint32_t st = sb + s * L::STAGE;
+      const uint32_t xt = st, wt = st + L::W_IN;
+      if constexpr (!BWD) {
+        // y = res*x + sum_k w[t,g,k] x[t-k]
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cch = 4 * h + q;
+          const int gl = cch * 8 / H;            // group of these 8 channels
+          float taps[W];
+#pragma unroll
+          for (int k = 0; k < W; ++k)
+            taps[k] = lds_bf16(wt + wtile_offset<L::WROW, L::WSW>(tl, (gl * W + k) * 2));
+          float xv[W][8];
+#pragma unroll
+          for (int k = 0; k < W; ++k)
+            unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch)), xv[k]);
+          float out[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float v = residual ? xv[0][c] : 0.f;
+#pragma unroll
+            for (int k = 0; k < W; ++k) v = fmaf(taps[k], xv[k][c], v);
+            out[c] = v;
+          }
+          sts128(obuf + sw128_offset(tl, cch), pack16<__nv_bfloat16>(out));
+        }
+      } else {
+        // dx = res*dy + sum_k w[t+k,g,k] dy[t+k];  dw[t,g,k] = sum_{c in g} dy[t,c] x[t-k,c]
+        const uint32_t dyt = st + L::DY_IN;
+        float p[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) p[k] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cch = 4 * h + q;
+          const int gl = cch * 8 / H;
+          float wk[W];
+#pragma unroll
+          for (int k = 0; k < W; ++k)
+            wk[k] = lds_bf16(wt + wtile_offset<L::WROW, L::WSW>(tl + k, (gl * W + k) * 2));
+          float gv[W][8];
+#pragma unroll
+          for (int k = 0; k < W; ++k)
+            unpack16<__nv_bfloat16>(lds128(dyt + sw128_offset(tl + k, cch)), gv[k]);
+          float out[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float v = residual ? gv[0][c] : 0.f;
+#pragma unroll
+            for (int k = 0; k < W; ++k) v = fmaf(wk[k], gv[k][c], v);
+            out[c] = v;
+          }
+          sts128(obuf + sw128_offset(tl, cch), pack16<__nv_bfloat16>(out));
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            float xv[8];
+            unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch)), xv);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) p[k] = fmaf(gv[0][c], xv[c], p[k]);
+          }
+          // The last 8-channel piece of a group: its W taps are complete.
+          if (((cch + 1) * 8) % H == 0) {
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+              sts_bf16(dwbuf + wtile_offset<L::WROW, L::WSW>(tl, (gl * W + k) * 2), p[k]);
+              p[k] = 0.f;
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_empty + 8 * s);
+        mbar_arrive(bar_ofull + 8 * g);
+      }
+      if (storer && mbar_wait(bar_ofull + 8 * g, aph, abort_flag, &g_hw_error, 4)) {
+        const HwItem itm =
+            hw_decode(blockIdx.x + static_cast<long long>(it) * gridDim.x, nchunks, ntiles);
+        tma_store_3d(&tm_out, obuf, itm.chunk * CC, itm.t0, itm.b, pol);
+        if constexpr (BWD) tma_store_3d(&tm_dw, dwbuf, itm.chunk * L::GI * W, itm.t0, itm.b, pol);
+        bulk_commit();
+      }
+    }
+    if (storer) bulk_wait<0>();
+  }
+  __syncthreads();
+}
+
+template <int W, int H, bool BWD>
+cudaError_t launch(const void* x, const void* dy, const void* w, void* out, void* dw,
+                   const Shape& s, cudaStream_t st) {
+  using L = HwLayout<W, H, BWD>;
+  const uint64_t GW = static_cast<uint64_t>(s.C / H) * W;
+  CUtensorMap tx, tdy, tw, tout, tdw;
+  if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
+      !make_tmap_3d(&tw, w, true, GW, s.T, s.B, L::GI * W, L::WROWS, L::WSW) ||
+      !make_tmap_3d(&tout, out, true, s.C, s.T, s.B, CC, BM, 128))
+    return cudaErrorInvalidValue;
+  if constexpr (BWD) {
+    if (!make_tmap_3d(&tdy, dy, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
+        !make_tmap_3d(&tdw, dw, true, GW, s.T, s.B, L::GI * W, BM, L::WSW))
+      return cudaErrorInvalidValue;
+  } else {
+    tdy = tx;
+    tdw = tw;
+  }
+  const int ntiles = static_cast<int>((s.T + BM - 1) / BM);
+  const int nchunks = static_cast<int>((s.C + CC - 1) / CC);
+  const long long nbt = static_cast<long long>(s.B) * ntiles;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorNoDevice;
+  const long long grid = std::min<long long>(sms, nbt * nchunks);
+  auto kern = hw_tma_kernel<W, H, BWD>;
+  cudaError_t e = set_smem<L>(kern, L::TOTAL);
+  if (e != cudaSuccess) return e;
+  kern<<<static_cast<unsigned>(grid), kThreads, L::TOTAL, st>>>(
+      tx, tdy, tw, tout, tdw, ntiles, static_cast<int>(nbt), nchunks, s.residual);
+  return cudaGetLastError();
+}
+
+// The (W, H) pairs whose w rows make a legal TMA box (a multiple of 16 bytes
+// for the chunk's 64/H groups x W taps): H = 8 with any W, H = 16 with
+// W = 2 or 4, H = 32 with W = 4.
+template <bool BWD>
+cudaError_t dispatch(const void* x, const void* dy, const void* w, void* out, void* dw,
+                     const Shape& s, cudaStream_t st) {
+  switch (s.H * 8 + s.W) {
+    case 8 * 8 + 1: return launch<1, 8, BWD>(x, dy, w, out, dw, s, st);
+    case 8 * 8 + 2: return launch<2, 8, BWD>(x, dy, w, out, dw, s, st);
+    case 8 * 8 + 3: return launch<3, 8, BWD>(x, dy, w, out, dw, s, st);
+    case 8 * 8 + 4: return launch<4, 8, BWD>(x, dy, w, out, dw, s, st);
+    case 16 * 8 + 2: return launch<2, 16, BWD>(x, dy, w, out, dw, s, st);
+    case 16 * 8 + 4: return launch<4, 16, BWD>(x, dy, w, out, dw, s, st);
+    case 32 * 8 + 4: return launch<4, 32, BWD>(x, dy, w, out, dw, s, st);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace
+
+bool headwise_tma_supported(const Shape& s) {
+  if (!s.bf16) return false;
+  const bool pair = (s.H == 8 && s.W >= 1 && s.W <= 4) || (s.H == 16 && (s.W == 2 || s.W == 4)) ||
+                    (s.H == 32 && s.W == 4);
+  return pair && s.C % 64 == 0 && s.T < (int64_t(1) << 30) &&
+         s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.C < (int64_t(1) << 24);
+}
+
+cudaError_t headwise_fwd_tma(const void* x, const void* w, void* y, const Shape& s,
+                             cudaStream_t st) {
+  if (!headwise_tma_supported(s)) return cudaErrorNotSupported;
+  return dispatch<false>(x, nullptr, w, y, nullptr, s, st);
+}
+
+cudaError_t headwise_bwd_tma(const void* x, const void* w, const void* dy, void* dx, void* dw,
+                             const Shape& s, cudaStream_t st) {
+  if (!headwise_tma_supported(s)) return cudaErrorNotSupported;
+  return dispatch<true>(x, dy, w, dx, dw, s, st);
+}
+
+cudaError_t headwise_tma_error(unsigned int* out, bool reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_hw_error, sizeof(unsigned int));
+  if (e != cudaSuccess || !reset) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_hw_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace dsc

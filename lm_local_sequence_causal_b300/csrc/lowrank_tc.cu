@@ -96,10 +96,6 @@ struct FwdLayout {
   static constexpr uint32_t TX = XBOX + KS * ZBYTES + UBYTES;  // bytes landing per stage
 };
 
-__device__ __forceinline__ unsigned char* align1k(unsigned char* p) {
-  return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                          ~static_cast<uintptr_t>(1023));
-}
 
 // Work item i of the forward -> (b, token tile, chunk): tile-major, so the
 // CTAs working side by side (items i, i+1, ... handed out round-robin) read
@@ -129,13 +125,6 @@ __device__ __forceinline__ uint32_t f2bf(float2 v) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Wait for a phase during teardown: ignores the abort flag, bounded in time.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return;
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > kWaitLimitNs) return;
-}
 
 // Shared-memory descriptor (fields as in sm100.cuh); layout 0 = no swizzle
 // (8-row x 16-byte core matrices), 2 = 128-byte swizzle, 6 = 32-byte swizzle.
@@ -882,25 +871,6 @@ __global__ void lr_reduce_tc(const float* __restrict__ dz_part, const float* __r
 
 // ------------------------------------------------------------------ host ----
 
-// Opt in to large dynamic shared memory, once per kernel and device.  The
-// template parameter `Tag` keeps one record per kernel instance (all
-// instances share a function type, so the type alone cannot tell them apart).
-template <typename Tag, typename F>
-cudaError_t set_smem(F* kernel, int bytes) {
-  static std::mutex mu;
-  static bool done[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!done[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    done[dev] = true;
-  }
-  return cudaSuccess;
-}
 
 template <int W, int KS>
 cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, const Shape& s,

@@ -54,6 +54,8 @@ def load():
                                     I64, INT, INT, P]
     lib.dsc_lowrank_uses_tensor_cores.argtypes = [I64, I64, I64, I64, I64, I64, INT]
     lib.dsc_lowrank_uses_tensor_cores.restype = INT
+    lib.dsc_headwise_uses_tma.argtypes = [I64, I64, I64, I64, I64, INT]
+    lib.dsc_headwise_uses_tma.restype = INT
     lib.dsc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), INT]
     lib.dsc_device_error.restype = INT
     for f in ("dsc_headwise_fwd", "dsc_headwise_bwd", "dsc_lowrank_fwd", "dsc_lowrank_bwd"):
@@ -73,6 +75,11 @@ def abi_version() -> int:
 def dsc_lowrank_uses_tensor_cores(B, T, C, H, W, R, dtype) -> int:
     """Bit 0: forward on the tensor cores, bit 1: backward; -1: invalid/unsupported."""
     return int(load().dsc_lowrank_uses_tensor_cores(B, T, C, H, W, R, _DTYPES[dtype]))
+
+
+def dsc_headwise_uses_tma(B, T, C, H, W, dtype) -> int:
+    """1: TMA-staged head-wise kernels, 0: register-streaming ones, -1: invalid."""
+    return int(load().dsc_headwise_uses_tma(B, T, C, H, W, _DTYPES[dtype]))
 
 
 def dsc_device_error(reset=False) -> int:

@@ -1,0 +1,72 @@
+"""GPU parity of the TMA-staged head-wise kernels against the fp64 oracle.
+
+These shapes take the TMA path (bf16, C a multiple of 64, (H, W) with a
+legal filter box); each case first checks that the library routes it there,
+and every test checks that no bounded wait in those kernels gave up.  The
+wider grid of H and W in test_parity_headwise.py also runs through this path
+for the same (H, W) pairs.
+"""
+import pytest
+import torch
+
+import oracle as orc
+from lm_local_sequence_causal_b300 import dsc, synthetic as syn
+from _parity import Guarded, assert_fwd, assert_grad
+
+pytestmark = pytest.mark.gpu
+
+TMA_PAIRS = [(8, 1), (8, 2), (8, 3), (8, 4), (16, 2), (16, 4), (32, 4)]
+
+
+@pytest.fixture(autouse=True)
+def no_device_error():
+    dsc.dsc_device_error(reset=True)
+    yield
+    torch.cuda.synchronize()
+    assert dsc.dsc_device_error() == 0, "a bounded wait in the TMA kernels gave up"
+
+
+def check(wl, seed):
+    assert dsc.dsc_headwise_uses_tma(wl.B, wl.T, wl.C, wl.H, wl.W, wl.dtype) == 1
+    inp = syn.make_inputs(wl, seed, device="cuda")
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+    y, dx, dw = Guarded(x.shape, wl.dtype), Guarded(x.shape, wl.dtype), Guarded(w.shape, wl.dtype)
+    dsc.dsc_headwise_fwd(x, w, y.t, wl.H, wl.residual)
+    dsc.dsc_headwise_bwd(x, w, dy, dx.t, dw.t, wl.H, wl.residual)
+    torch.cuda.synchronize()
+    for o, n in ((y, "y"), (dx, "dx"), (dw, "dw")):
+        assert o.guards_intact(), f"{n}: write outside the tensor"
+    ry = orc.headwise_fwd(x, w, wl.H, wl.residual)
+    rdx, rdw = orc.headwise_bwd(x, w, dy, wl.H, wl.residual)
+    assert_fwd(y.t, ry, wl.dtype)
+    assert_grad(dx.t, rdx, wl.dtype, "dx")
+    assert_grad(dw.t, rdw, wl.dtype, "dw")
+
+
+@pytest.mark.parametrize("H,W", TMA_PAIRS)
+@pytest.mark.parametrize("residual", [False, True])
+def test_every_legal_group_size_and_width(H, W, residual):
+    wl = syn.Workload("hw_tma", B=2, T=300, C=320, W=W, H=H, residual=residual)
+    check(wl, seed=H * 10 + W + 100 * residual)
+
+
+@pytest.mark.parametrize("T", [1, 3, 4, 127, 128, 129, 131, 257])
+def test_short_and_ragged_sequences(T):
+    wl = syn.Workload("hw_tma_T", B=3, T=T, C=192, W=4, H=16)
+    check(wl, seed=T)
+
+
+def test_many_items_per_cta():
+    wl = syn.Workload("hw_tma_big", B=4, T=1024, C=2048, W=4, H=16)
+    check(wl, seed=5)
+
+
+def test_routing():
+    q = dsc.dsc_headwise_uses_tma
+    bf = torch.bfloat16
+    assert q(8, 2048, 6144, 16, 4, bf) == 1           # the QKV placement
+    assert q(8, 2048, 6144, 16, 3, bf) == 0           # W = 3 taps are not a 16-byte box
+    assert q(2, 16384, 4096, 64, 4, bf) == 0          # one group per 64 channels: 8-byte box
+    assert q(8, 2048, 6144, 16, 4, torch.float32) == 0
+    assert q(8, 2048, 6120, 8, 4, bf) == 0            # C not a multiple of 64
+    assert q(8, 2048, 6144, 16, 5, bf) == -1
