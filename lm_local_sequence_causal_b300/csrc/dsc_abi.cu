@@ -164,7 +164,9 @@ dsc_status_t dsc_device_error(unsigned int* code, int reset) {
 int dsc_headwise_uses_tma(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
                           dsc_dtype_t dtype) {
   if (check_shape(B, T, C, H, W, 0, dtype, false) != DSC_OK) return -1;
-  return dsc::headwise_tma_supported(make_shape(B, T, C, H, W, 0, 0, dtype)) ? 1 : 0;
+  const Shape s = make_shape(B, T, C, H, W, 0, 0, dtype);
+  return (dsc::headwise_tma_supported(s, false) ? 1 : 0) |
+         (dsc::headwise_tma_supported(s, true) ? 2 : 0);
 }
 
 }  // extern "C"

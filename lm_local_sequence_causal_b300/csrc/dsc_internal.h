@@ -25,9 +25,10 @@ cudaError_t headwise_fwd(const void* x, const void* w, void* y, const Shape& s,
 cudaError_t headwise_bwd(const void* x, const void* w, const void* dy, void* dx,
                          void* dw, const Shape& s, cudaStream_t st);
 
-// Head-wise kernels with TMA-staged tiles (headwise_tma.cu): bf16, C % 64
-// == 0 and (H, W) in {(8, any), (16, 2), (16, 4), (32, 4)}.
-bool headwise_tma_supported(const Shape& s);
+// Head-wise kernels with TMA-staged tiles (headwise_tma.cu): bf16 and the
+// (H, W) pairs whose filter rows make a legal TMA box, C a multiple of the
+// item width (64 or 128 channels).
+bool headwise_tma_supported(const Shape& s, bool bwd);
 cudaError_t headwise_fwd_tma(const void* x, const void* w, void* y, const Shape& s,
                              cudaStream_t st);
 cudaError_t headwise_bwd_tma(const void* x, const void* w, const void* dy, void* dx, void* dw,

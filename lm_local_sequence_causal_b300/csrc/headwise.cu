@@ -468,13 +468,13 @@ cudaError_t bwd_t(const void* x, const void* w, const void* dy, void* dx, void* 
 
 cudaError_t headwise_fwd(const void* x, const void* w, void* y, const Shape& s,
                          cudaStream_t st) {
-  if (headwise_tma_supported(s)) return headwise_fwd_tma(x, w, y, s, st);
+  if (headwise_tma_supported(s, false)) return headwise_fwd_tma(x, w, y, s, st);
   return s.bf16 ? fwd_t<__nv_bfloat16>(x, w, y, s, st) : fwd_t<float>(x, w, y, s, st);
 }
 
 cudaError_t headwise_bwd(const void* x, const void* w, const void* dy, void* dx,
                          void* dw, const Shape& s, cudaStream_t st) {
-  if (headwise_tma_supported(s)) return headwise_bwd_tma(x, w, dy, dx, dw, s, st);
+  if (headwise_tma_supported(s, true)) return headwise_bwd_tma(x, w, dy, dx, dw, s, st);
   return s.bf16 ? bwd_t<__nv_bfloat16>(x, w, dy, dx, dw, s, st)
                 : bwd_t<float>(x, w, dy, dx, dw, s, st);
 }

@@ -1,5 +1,5 @@
 // headwise_tma.cu -- head-wise Dynamic Short Convolution, forward and backward,
-// with TMA-staged tiles (bf16, H in {8, 16, 32}).
+// with TMA-staged tiles (bf16; the (H, W) pairs listed at `dispatch`).
 //
 // y[b,t,c] = res*x[b,t,c] + sum_{k<W} w[b,t,c/H,k] * x[b,t-k,c]   (x = 0 before t = 0)
 // ("Technische Samenvatting: Dynamische Korte Convoluties Verbeteren
@@ -8,19 +8,20 @@
 //   dx[b,s,c]   = res*dy[b,s,c] + sum_{k: s+k<T} w[b,s+k,c/H,k] dy[b,s+k,c]
 //   dw[b,t,g,k] = sum_{c in group g} dy[b,t,c] x[b,t-k,c]
 //
-// Pure streams over HBM.  A work item is (b, 128-token tile, 64-channel
-// chunk); one persistent CTA per SM takes items round-robin in tile-major
-// order, so neighbouring CTAs read neighbouring pieces of the same rows.
+// Pure streams over HBM.  A work item is (b, 128-token tile, chunk of 64 or
+// 128 channels); one persistent CTA per SM takes items round-robin in
+// tile-major order, so neighbouring CTAs read neighbouring pieces of the
+// same rows.
 //   warp 0      TMA producer, 4-stage ring: x rows [t0-W+1, t0+128) (the
 //               rows before t = 0 read as zero: the causal padding), in the
 //               backward also dy rows and w rows [t0, t0+127+W) (rows past T
 //               read as zero, which drops the terms with s+k >= T), and the
-//               w rows of the tile: the chunk's 64/H groups x W taps.
+//               w rows of the tile: the chunk's groups x W taps.
 //   warps 1-16  two independent groups of 8 warps that take alternate items,
 //               each with its own staged output tiles; in a group the warp
 //               (lane group lg = w % 4, half h) owns tokens 32*lg .. +31 and
-//               channels 32*h .. +31 of the chunk (four 8-channel pieces,
-//               which are whole groups since H >= 8).  Outputs go to staged
+//               half of the chunk's channels (8-channel pieces, which make
+//               whole groups since H >= 8).  Outputs go to staged
 //               tiles that one thread of the group stores with TMA.
 // Every mbarrier wait is bounded (sm100.cuh); a timeout records a code in
 // this file's device error word and the CTA returns.
@@ -41,30 +42,33 @@ using namespace sm100;
 __device__ unsigned int g_hw_error = 0;
 
 constexpr int BM = 128;      // tokens per tile
-constexpr int CC = 64;       // channels per chunk (one 128-byte swizzled row)
-constexpr int NST = 4;       // input pipeline stages
 constexpr int NGRP = 8;      // warps per epilogue group
 constexpr int kThreads = (1 + 2 * NGRP) * 32;
 
 __host__ __device__ constexpr int round1k(int b) { return (b + 1023) / 1024 * 1024; }
 
-// Shared-memory layout of one configuration.  BWD adds the dy box and a
-// longer w box (the dx terms need w[s+k]) and the staged dw tile.
-template <int W, int H, bool BWD>
+// Shared-memory layout of one configuration: items of 128 tokens x CW
+// channels (CW = 64 or 128; x, dy and outputs move as CW/64 boxes of 64
+// channels with 128-byte swizzle).  BWD adds the dy boxes, a longer w box
+// (the dx terms need w[s+k]) and the staged dw tile.
+template <int W, int H, bool BWD, int CW>
 struct HwLayout {
-  static constexpr int GI = CC / H;                  // groups per chunk
-  static constexpr int WROW = GI * W * 2;            // bytes of one token's taps
+  static constexpr int NB = CW / 64;                  // 64-channel boxes per item
+  static constexpr int NST = BWD ? (NB == 1 ? 4 : 2) : (NB == 1 ? 4 : 3);
+  static constexpr int GI = CW / H;                   // groups per item
+  static constexpr int WROW = GI * W * 2;             // bytes of one token's taps
   static constexpr int WSW = (WROW == 32 || WROW == 64) ? WROW : 0;  // swizzle of the w box
   static constexpr int XROWS = BM + W - 1;
-  static constexpr int XBOX = XROWS * 128;
+  static constexpr int XBOX = XROWS * 128;            // one 64-channel box
   static constexpr int XBYTES = round1k(XBOX);
   static constexpr int WROWS = BWD ? XROWS : BM;
   static constexpr int WBOX = WROWS * WROW;
   static constexpr int WBYTES = round1k(WBOX);
-  static constexpr int DY_IN = XBYTES;               // offsets inside a stage
-  static constexpr int W_IN = BWD ? 2 * XBYTES : XBYTES;
+  static constexpr int DY_IN = NB * XBYTES;           // offsets inside a stage
+  static constexpr int W_IN = (BWD ? 2 : 1) * NB * XBYTES;
   static constexpr int STAGE = W_IN + WBYTES;
-  static constexpr int OBYTES = BM * 128;            // staged y / dx tile of one group
+  static constexpr int OBOX = BM * 128;               // one staged 64-channel output box
+  static constexpr int OBYTES = NB * OBOX;            // staged y / dx tile of one group
   static constexpr int DWBYTES = BWD ? round1k(BM * WROW) : 0;  // staged dw tile of one group
   static constexpr int O_OFF = NST * STAGE;
   static constexpr int DW_OFF = O_OFF + 2 * OBYTES;
@@ -73,7 +77,7 @@ struct HwLayout {
   static constexpr int NBAR = 2 * NST + 4;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int TOTAL = MISC_OFF + 16 + 1024;
-  static constexpr uint32_t TX = (BWD ? 2 : 1) * XBOX + WBOX;
+  static constexpr uint32_t TX = (BWD ? 2 : 1) * NB * XBOX + WBOX;
 };
 
 // Byte offset of byte `o` of row `r` in a w tile of `row` bytes per row
@@ -109,13 +113,16 @@ __device__ __forceinline__ HwItem hw_decode(long long i, int nchunks, int ntiles
   return it;
 }
 
-template <int W, int H, bool BWD>
+template <int W, int H, bool BWD, int CW>
 __global__ void __launch_bounds__(kThreads, 1)
 hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_out,
               const __grid_constant__ CUtensorMap tm_dw, int ntiles, int nbt, int nchunks,
               int residual) {
-  using L = HwLayout<W, H, BWD>;
+  using L = HwLayout<W, H, BWD, CW>;
+  constexpr int NST = L::NST;
+  constexpr int NB = L::NB;
+  constexpr int PPW = CW / 16;                         // 8-channel pieces per warp
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1k(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -165,8 +172,14 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         const uint32_t full = bar_full + 8 * s;
         const uint32_t st = sb + s * L::STAGE;
         mbar_expect_tx(full, L::TX);
-        tma_load_3d(st, &tm_x, full, itm.chunk * CC, itm.t0 - (W - 1), itm.b, pol);
-        if constexpr (BWD) tma_load_3d(st + L::DY_IN, &tm_dy, full, itm.chunk * CC, itm.t0, itm.b, pol);
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          tma_load_3d(st + j * L::XBYTES, &tm_x, full, itm.chunk * CW + 64 * j, itm.t0 - (W - 1),
+                      itm.b, pol);
+          if constexpr (BWD)
+            tma_load_3d(st + L::DY_IN + j * L::XBYTES, &tm_dy, full, itm.chunk * CW + 64 * j,
+                        itm.t0, itm.b, pol);
+        }
         tma_load_3d(st + L::W_IN, &tm_w, full, itm.chunk * L::GI * W, itm.t0, itm.b, pol);
       }
       for (int j = std::max(0, it - NST); j < it; ++j)
@@ -193,13 +206,14 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                 mbar_wait(bar_full + 8 * s, (it / NST) & 1, abort_flag, &g_hw_error, 3);
       if (!__all_sync(0xffffffffu, ok)) break;
       const uint32_t st = sb + s * L::STAGE;
-      const uint32_t xt = st, wt = st + L::W_IN;
+      const uint32_t wt = st + L::W_IN;
       if constexpr (!BWD) {
         // y = res*x + sum_k w[t,g,k] x[t-k]
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int cch = 4 * h + q;
-          const int gl = cch * 8 / H;            // group of these 8 channels
+        for (int q = 0; q < PPW; ++q) {
+          const int cch = PPW * h + q;           // 8-channel piece of the item
+          const int gl = cch * 8 / H;            // its filter group within the item
+          const uint32_t xt = st + (cch >> 3) * L::XBYTES;
           float taps[W];
 #pragma unroll
           for (int k = 0; k < W; ++k)
@@ -207,7 +221,7 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
           float xv[W][8];
 #pragma unroll
           for (int k = 0; k < W; ++k)
-            unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch)), xv[k]);
+            unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch & 7)), xv[k]);
           float out[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -216,18 +230,20 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             for (int k = 0; k < W; ++k) v = fmaf(taps[k], xv[k][c], v);
             out[c] = v;
           }
-          sts128(obuf + sw128_offset(tl, cch), pack16<__nv_bfloat16>(out));
+          sts128(obuf + (cch >> 3) * L::OBOX + sw128_offset(tl, cch & 7),
+                 pack16<__nv_bfloat16>(out));
         }
       } else {
         // dx = res*dy + sum_k w[t+k,g,k] dy[t+k];  dw[t,g,k] = sum_{c in g} dy[t,c] x[t-k,c]
-        const uint32_t dyt = st + L::DY_IN;
         float p[W];
 #pragma unroll
         for (int k = 0; k < W; ++k) p[k] = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int cch = 4 * h + q;
+        for (int q = 0; q < PPW; ++q) {
+          const int cch = PPW * h + q;
           const int gl = cch * 8 / H;
+          const uint32_t xt = st + (cch >> 3) * L::XBYTES;
+          const uint32_t dyt = st + L::DY_IN + (cch >> 3) * L::XBYTES;
           float wk[W];
 #pragma unroll
           for (int k = 0; k < W; ++k)
@@ -235,7 +251,7 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
           float gv[W][8];
 #pragma unroll
           for (int k = 0; k < W; ++k)
-            unpack16<__nv_bfloat16>(lds128(dyt + sw128_offset(tl + k, cch)), gv[k]);
+            unpack16<__nv_bfloat16>(lds128(dyt + sw128_offset(tl + k, cch & 7)), gv[k]);
           float out[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -244,11 +260,12 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             for (int k = 0; k < W; ++k) v = fmaf(wk[k], gv[k][c], v);
             out[c] = v;
           }
-          sts128(obuf + sw128_offset(tl, cch), pack16<__nv_bfloat16>(out));
+          sts128(obuf + (cch >> 3) * L::OBOX + sw128_offset(tl, cch & 7),
+                 pack16<__nv_bfloat16>(out));
 #pragma unroll
           for (int k = 0; k < W; ++k) {
             float xv[8];
-            unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch)), xv);
+            unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch & 7)), xv);
 #pragma unroll
             for (int c = 0; c < 8; ++c) p[k] = fmaf(gv[0][c], xv[c], p[k]);
           }
@@ -271,7 +288,9 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
       if (storer && mbar_wait(bar_ofull + 8 * g, aph, abort_flag, &g_hw_error, 4)) {
         const HwItem itm =
             hw_decode(blockIdx.x + static_cast<long long>(it) * gridDim.x, nchunks, ntiles);
-        tma_store_3d(&tm_out, obuf, itm.chunk * CC, itm.t0, itm.b, pol);
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          tma_store_3d(&tm_out, obuf + j * L::OBOX, itm.chunk * CW + 64 * j, itm.t0, itm.b, pol);
         if constexpr (BWD) tma_store_3d(&tm_dw, dwbuf, itm.chunk * L::GI * W, itm.t0, itm.b, pol);
         bulk_commit();
       }
@@ -281,18 +300,18 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
   __syncthreads();
 }
 
-template <int W, int H, bool BWD>
+template <int W, int H, bool BWD, int CW>
 cudaError_t launch(const void* x, const void* dy, const void* w, void* out, void* dw,
                    const Shape& s, cudaStream_t st) {
-  using L = HwLayout<W, H, BWD>;
+  using L = HwLayout<W, H, BWD, CW>;
   const uint64_t GW = static_cast<uint64_t>(s.C / H) * W;
   CUtensorMap tx, tdy, tw, tout, tdw;
-  if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
+  if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, 64, L::XROWS, 128) ||
       !make_tmap_3d(&tw, w, true, GW, s.T, s.B, L::GI * W, L::WROWS, L::WSW) ||
-      !make_tmap_3d(&tout, out, true, s.C, s.T, s.B, CC, BM, 128))
+      !make_tmap_3d(&tout, out, true, s.C, s.T, s.B, 64, BM, 128))
     return cudaErrorInvalidValue;
   if constexpr (BWD) {
-    if (!make_tmap_3d(&tdy, dy, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
+    if (!make_tmap_3d(&tdy, dy, true, s.C, s.T, s.B, 64, L::XROWS, 128) ||
         !make_tmap_3d(&tdw, dw, true, GW, s.T, s.B, L::GI * W, BM, L::WSW))
       return cudaErrorInvalidValue;
   } else {
@@ -300,12 +319,12 @@ cudaError_t launch(const void* x, const void* dy, const void* w, void* out, void
     tdw = tw;
   }
   const int ntiles = static_cast<int>((s.T + BM - 1) / BM);
-  const int nchunks = static_cast<int>((s.C + CC - 1) / CC);
+  const int nchunks = static_cast<int>(s.C / CW);
   const long long nbt = static_cast<long long>(s.B) * ntiles;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   const long long grid = std::min<long long>(sms, nbt * nchunks);
-  auto kern = hw_tma_kernel<W, H, BWD>;
+  auto kern = hw_tma_kernel<W, H, BWD, CW>;
   cudaError_t e = set_smem<L>(kern, L::TOTAL);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kThreads, L::TOTAL, st>>>(
@@ -313,43 +332,63 @@ cudaError_t launch(const void* x, const void* dy, const void* w, void* out, void
   return cudaGetLastError();
 }
 
-// The (W, H) pairs whose w rows make a legal TMA box (a multiple of 16 bytes
-// for the chunk's 64/H groups x W taps): H = 8 with any W, H = 16 with
-// W = 2 or 4, H = 32 with W = 4.
+// The (H, W) pairs whose filter rows make a legal TMA box (a multiple of 16
+// bytes for the item's CW/H groups x W taps), with the narrowest item that
+// does: 64 channels for H = 8 (any W), (16, 2), (16, 4), (32, 4); 128
+// channels for (16, 1), (16, 3), (32, 2), (64, 4).
 template <bool BWD>
 cudaError_t dispatch(const void* x, const void* dy, const void* w, void* out, void* dw,
                      const Shape& s, cudaStream_t st) {
   switch (s.H * 8 + s.W) {
-    case 8 * 8 + 1: return launch<1, 8, BWD>(x, dy, w, out, dw, s, st);
-    case 8 * 8 + 2: return launch<2, 8, BWD>(x, dy, w, out, dw, s, st);
-    case 8 * 8 + 3: return launch<3, 8, BWD>(x, dy, w, out, dw, s, st);
-    case 8 * 8 + 4: return launch<4, 8, BWD>(x, dy, w, out, dw, s, st);
-    case 16 * 8 + 2: return launch<2, 16, BWD>(x, dy, w, out, dw, s, st);
-    case 16 * 8 + 4: return launch<4, 16, BWD>(x, dy, w, out, dw, s, st);
-    case 32 * 8 + 4: return launch<4, 32, BWD>(x, dy, w, out, dw, s, st);
+    case 8 * 8 + 1: return launch<1, 8, BWD, 64>(x, dy, w, out, dw, s, st);
+    case 8 * 8 + 2: return launch<2, 8, BWD, 64>(x, dy, w, out, dw, s, st);
+    case 8 * 8 + 3: return launch<3, 8, BWD, 64>(x, dy, w, out, dw, s, st);
+    case 8 * 8 + 4: return launch<4, 8, BWD, 64>(x, dy, w, out, dw, s, st);
+    case 16 * 8 + 1: return launch<1, 16, BWD, 128>(x, dy, w, out, dw, s, st);
+    case 16 * 8 + 2: return launch<2, 16, BWD, 64>(x, dy, w, out, dw, s, st);
+    case 16 * 8 + 3:
+      if constexpr (!BWD) return launch<3, 16, BWD, 128>(x, dy, w, out, dw, s, st);
+      return cudaErrorNotSupported;
+    case 16 * 8 + 4: return launch<4, 16, BWD, 64>(x, dy, w, out, dw, s, st);
+    case 32 * 8 + 2: return launch<2, 32, BWD, 128>(x, dy, w, out, dw, s, st);
+    case 32 * 8 + 4: return launch<4, 32, BWD, 64>(x, dy, w, out, dw, s, st);
+    case 64 * 8 + 4: return launch<4, 64, BWD, 128>(x, dy, w, out, dw, s, st);
     default: return cudaErrorNotSupported;
   }
 }
 
+// Channel width of the item for (H, W), 0 if the pair has no TMA path.  The
+// backward of (16, 3) has none: with 48-byte filter rows its two stages,
+// two staged outputs and two staged dw tiles do not fit shared memory.
+int item_width(int64_t H, int64_t W, bool bwd) {
+  if (bwd && H == 16 && W == 3) return 0;
+  if (H == 8 && W >= 1 && W <= 4) return 64;
+  if (H == 16 && (W == 2 || W == 4)) return 64;
+  if (H == 16 && (W == 1 || W == 3)) return 128;
+  if (H == 32 && W == 4) return 64;
+  if (H == 32 && W == 2) return 128;
+  if (H == 64 && W == 4) return 128;
+  return 0;
+}
+
 }  // namespace
 
-bool headwise_tma_supported(const Shape& s) {
+bool headwise_tma_supported(const Shape& s, bool bwd) {
   if (!s.bf16) return false;
-  const bool pair = (s.H == 8 && s.W >= 1 && s.W <= 4) || (s.H == 16 && (s.W == 2 || s.W == 4)) ||
-                    (s.H == 32 && s.W == 4);
-  return pair && s.C % 64 == 0 && s.T < (int64_t(1) << 30) &&
+  const int cw = item_width(s.H, s.W, bwd);
+  return cw > 0 && s.C % cw == 0 && s.T < (int64_t(1) << 30) &&
          s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.C < (int64_t(1) << 24);
 }
 
 cudaError_t headwise_fwd_tma(const void* x, const void* w, void* y, const Shape& s,
                              cudaStream_t st) {
-  if (!headwise_tma_supported(s)) return cudaErrorNotSupported;
+  if (!headwise_tma_supported(s, false)) return cudaErrorNotSupported;
   return dispatch<false>(x, nullptr, w, y, nullptr, s, st);
 }
 
 cudaError_t headwise_bwd_tma(const void* x, const void* w, const void* dy, void* dx, void* dw,
                              const Shape& s, cudaStream_t st) {
-  if (!headwise_tma_supported(s)) return cudaErrorNotSupported;
+  if (!headwise_tma_supported(s, true)) return cudaErrorNotSupported;
   return dispatch<true>(x, dy, w, dx, dw, s, st);
 }
 

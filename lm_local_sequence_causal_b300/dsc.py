@@ -78,7 +78,7 @@ def dsc_lowrank_uses_tensor_cores(B, T, C, H, W, R, dtype) -> int:
 
 
 def dsc_headwise_uses_tma(B, T, C, H, W, dtype) -> int:
-    """1: TMA-staged head-wise kernels, 0: register-streaming ones, -1: invalid."""
+    """Bit 0: forward on the TMA-staged kernel, bit 1: backward; -1: invalid."""
     return int(load().dsc_headwise_uses_tma(B, T, C, H, W, _DTYPES[dtype]))
 
 

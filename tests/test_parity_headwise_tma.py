@@ -15,7 +15,9 @@ from _parity import Guarded, assert_fwd, assert_grad
 
 pytestmark = pytest.mark.gpu
 
-TMA_PAIRS = [(8, 1), (8, 2), (8, 3), (8, 4), (16, 2), (16, 4), (32, 4)]
+# (H, W, item width in channels)
+TMA_PAIRS = [(8, 1, 64), (8, 2, 64), (8, 3, 64), (8, 4, 64), (16, 2, 64), (16, 4, 64),
+             (32, 4, 64), (16, 1, 128), (32, 2, 128), (64, 4, 128)]
 
 
 @pytest.fixture(autouse=True)
@@ -26,8 +28,8 @@ def no_device_error():
     assert dsc.dsc_device_error() == 0, "a bounded wait in the TMA kernels gave up"
 
 
-def check(wl, seed):
-    assert dsc.dsc_headwise_uses_tma(wl.B, wl.T, wl.C, wl.H, wl.W, wl.dtype) == 1
+def check(wl, seed, paths=3):
+    assert dsc.dsc_headwise_uses_tma(wl.B, wl.T, wl.C, wl.H, wl.W, wl.dtype) == paths
     inp = syn.make_inputs(wl, seed, device="cuda")
     x, w, dy = inp["x"], inp["w"], inp["dy"]
     y, dx, dw = Guarded(x.shape, wl.dtype), Guarded(x.shape, wl.dtype), Guarded(w.shape, wl.dtype)
@@ -43,11 +45,23 @@ def check(wl, seed):
     assert_grad(dw.t, rdw, wl.dtype, "dw")
 
 
-@pytest.mark.parametrize("H,W", TMA_PAIRS)
+@pytest.mark.parametrize("H,W,CW", TMA_PAIRS)
 @pytest.mark.parametrize("residual", [False, True])
-def test_every_legal_group_size_and_width(H, W, residual):
-    wl = syn.Workload("hw_tma", B=2, T=300, C=320, W=W, H=H, residual=residual)
+def test_every_legal_group_size_and_width(H, W, CW, residual):
+    wl = syn.Workload("hw_tma", B=2, T=300, C=5 * CW, W=W, H=H, residual=residual)
     check(wl, seed=H * 10 + W + 100 * residual)
+
+
+def test_w3_h16_forward_on_tma_backward_streaming():
+    # the all-linear sweep's H = 16, W = 3: forward on TMA, backward on the
+    # register-streaming kernel (its TMA tiles would not fit shared memory)
+    wl = syn.Workload("hw_tma_w3", B=2, T=300, C=640, W=3, H=16)
+    check(wl, seed=33, paths=1)
+
+
+def test_linear_rnn_shape_on_tma():
+    wl = syn.Workload("hw_tma_rnn", B=1, T=1100, C=512, W=4, H=64, hot_frac=0.05)
+    check(wl, seed=64)
 
 
 @pytest.mark.parametrize("T", [1, 3, 4, 127, 128, 129, 131, 257])
@@ -64,9 +78,10 @@ def test_many_items_per_cta():
 def test_routing():
     q = dsc.dsc_headwise_uses_tma
     bf = torch.bfloat16
-    assert q(8, 2048, 6144, 16, 4, bf) == 1           # the QKV placement
-    assert q(8, 2048, 6144, 16, 3, bf) == 0           # W = 3 taps are not a 16-byte box
-    assert q(2, 16384, 4096, 64, 4, bf) == 0          # one group per 64 channels: 8-byte box
+    assert q(8, 2048, 6144, 16, 4, bf) == 3           # the QKV placement
+    assert q(8, 2048, 6144, 16, 3, bf) == 1           # forward only (128-channel items)
+    assert q(2, 16384, 4096, 64, 4, bf) == 3          # linear-RNN shape (128-channel items)
+    assert q(8, 2048, 6144, 64, 3, bf) == 0           # 6-tap rows: no legal box
     assert q(8, 2048, 6144, 16, 4, torch.float32) == 0
     assert q(8, 2048, 6120, 8, 4, bf) == 0            # C not a multiple of 64
     assert q(8, 2048, 6144, 16, 5, bf) == -1
