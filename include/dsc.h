@@ -136,6 +136,36 @@ dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U,
                              dsc_dtype_t dtype, void* stream);
 
 /*
+ * Decode step (inference, one new token per sequence) with a carried state.
+ * The pages leave inference to future engineering; this is the forward
+ * definition evaluated at one new position t with the last W-1 inputs of
+ * each sequence kept as state:
+ *   y[b,c]        = residual*x[b,c] + w[b,g(c),0] x[b,c]
+ *                   + sum_{k=1}^{W-1} w[b,g(c),k] state[b,k-1,c]
+ *   state[b,0,c] <- x[b,c],  state[b,j,c] <- state[b,j-1,c]   (j >= 1)
+ * where state[b,j] holds the input at time t-1-j (all zeros at the start of
+ * a sequence, the causal zero padding).
+ *   x, y  : [B, C]          w : [B, C/H, W]
+ *   state : [B, W-1, C], read and updated in place (may be NULL when W = 1)
+ * Same element type for all; arithmetic fp32, y rounded once; the state
+ * keeps exact copies of the inputs.  y may not alias x, state may not alias
+ * x or y.  Alignment, shape and error rules as for the other entry points
+ * (T is 1); B = 0 is a no-op.
+ */
+dsc_status_t dsc_headwise_decode(const void* x, const void* w, void* state, void* y,
+                                 int64_t B, int64_t C, int64_t H, int64_t W, int residual,
+                                 dsc_dtype_t dtype, void* stream);
+
+/*
+ * Low-rank decode step: the taps w[b,g,k] = sum_r z[b,r] U[r,g*W+k] are
+ * formed in fp32 (never rounded), then the step above.  z : [B, R],
+ * U : [R, (C/H)*W], 1 <= R <= 32.
+ */
+dsc_status_t dsc_lowrank_decode(const void* x, const void* z, const void* U, void* state,
+                                void* y, int64_t B, int64_t C, int64_t H, int64_t W, int64_t R,
+                                int residual, dsc_dtype_t dtype, void* stream);
+
+/*
  * Which low-rank kernels these arguments run on: bit 0 set if
  * dsc_lowrank_fwd uses the tensor cores (tcgen05: bf16, H = 1, R = 16 or
  * 32, 1 <= W <= 4), bit 1 set if dsc_lowrank_bwd does (bf16, H = 1,

@@ -144,6 +144,35 @@ dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U, const 
                                     (cudaStream_t)stream));
 }
 
+dsc_status_t dsc_headwise_decode(const void* x, const void* w, void* state, void* y, int64_t B,
+                                 int64_t C, int64_t H, int64_t W, int residual,
+                                 dsc_dtype_t dtype, void* stream) {
+  dsc_status_t st = check_shape(B, 1, C, H, W, 0, dtype, false);
+  if (st != DSC_OK) return st;
+  if (B == 0) return DSC_OK;
+  if ((st = check_ptrs({x, w, y})) != DSC_OK) return st;
+  if (W > 1 && (st = check_ptrs({state})) != DSC_OK) return st;
+  if (y == x || (W > 1 && (state == x || state == y))) return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::headwise_decode(x, w, state, y,
+                                        make_shape(B, 1, C, H, W, 0, residual, dtype),
+                                        (cudaStream_t)stream));
+}
+
+dsc_status_t dsc_lowrank_decode(const void* x, const void* z, const void* U, void* state,
+                                void* y, int64_t B, int64_t C, int64_t H, int64_t W, int64_t R,
+                                int residual, dsc_dtype_t dtype, void* stream) {
+  dsc_status_t st = check_shape(B, 1, C, H, W, R, dtype, true);
+  if (st != DSC_OK) return st;
+  if (R > 32) return DSC_ERR_UNSUPPORTED;
+  if (B == 0) return DSC_OK;
+  if ((st = check_ptrs({x, z, U, y})) != DSC_OK) return st;
+  if (W > 1 && (st = check_ptrs({state})) != DSC_OK) return st;
+  if (y == x || (W > 1 && (state == x || state == y))) return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::lowrank_decode(x, z, U, state, y,
+                                       make_shape(B, 1, C, H, W, R, residual, dtype),
+                                       (cudaStream_t)stream));
+}
+
 int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
                                   int64_t R, dsc_dtype_t dtype) {
   if (check_shape(B, T, C, H, W, R, dtype, true) != DSC_OK) return -1;

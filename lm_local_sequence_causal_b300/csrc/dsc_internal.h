@@ -35,6 +35,12 @@ cudaError_t headwise_bwd_tma(const void* x, const void* w, const void* dy, void*
                              const Shape& s, cudaStream_t st);
 cudaError_t headwise_tma_error(unsigned int* out, bool reset);
 
+// Decode step with a carried state (decode.cu).
+cudaError_t headwise_decode(const void* x, const void* w, void* state, void* y, const Shape& s,
+                            cudaStream_t st);
+cudaError_t lowrank_decode(const void* x, const void* z, const void* U, void* state, void* y,
+                           const Shape& s, cudaStream_t st);
+
 // Low-rank kernels (lowrank_simt.cu).
 bool lowrank_supported(const Shape& s);
 cudaError_t lowrank_fwd(const void* x, const void* z, const void* U, void* y,

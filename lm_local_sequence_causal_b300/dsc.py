@@ -52,6 +52,10 @@ def load():
     lib.dsc_lowrank_bwd_workspace_size.restype = SZ
     lib.dsc_lowrank_bwd.argtypes = [P, P, P, P, P, P, P, P, SZ, I64, I64, I64, I64, I64,
                                     I64, INT, INT, P]
+    lib.dsc_headwise_decode.argtypes = [P, P, P, P, I64, I64, I64, I64, INT, INT, P]
+    lib.dsc_lowrank_decode.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, INT, INT, P]
+    lib.dsc_headwise_decode.restype = INT
+    lib.dsc_lowrank_decode.restype = INT
     lib.dsc_lowrank_uses_tensor_cores.argtypes = [I64, I64, I64, I64, I64, I64, INT]
     lib.dsc_lowrank_uses_tensor_cores.restype = INT
     lib.dsc_headwise_uses_tma.argtypes = [I64, I64, I64, I64, I64, INT]
@@ -177,6 +181,33 @@ def dsc_lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, H, W, residual=True, str
                                   _ptr(dU, dt, "dU"), ws_ptr, ws_bytes, B, T, C, H, W, R,
                                   int(bool(residual)), _dtype_code(x), _stream(stream)),
            "dsc_lowrank_bwd")
+
+
+def dsc_headwise_decode(x, w, state, y, H, residual=True, stream=None):
+    """One decode step: y [B,C] from x [B,C], w [B,G,W] and state [B,W-1,C]
+    (updated in place to hold the last W-1 inputs, newest first)."""
+    if x.dim() != 2:
+        raise ValueError("x must be [B, C]")
+    B, C = x.shape
+    W = w.shape[-1]
+    dt = x.dtype
+    sp = _ptr(state, dt, "state") if W > 1 else None
+    _check(load().dsc_headwise_decode(_ptr(x, dt, "x"), _ptr(w, dt, "w"), sp, _ptr(y, dt, "y"),
+                                      B, C, H, W, int(bool(residual)), _dtype_code(x),
+                                      _stream(stream)), "dsc_headwise_decode")
+
+
+def dsc_lowrank_decode(x, z, U, state, y, H, W, residual=True, stream=None):
+    """Low-rank decode step: taps z [B,R] U formed in fp32, then as above."""
+    if x.dim() != 2:
+        raise ValueError("x must be [B, C]")
+    B, C = x.shape
+    R = z.shape[-1]
+    dt = x.dtype
+    sp = _ptr(state, dt, "state") if W > 1 else None
+    _check(load().dsc_lowrank_decode(_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"), sp,
+                                     _ptr(y, dt, "y"), B, C, H, W, R, int(bool(residual)),
+                                     _dtype_code(x), _stream(stream)), "dsc_lowrank_decode")
 
 
 # ------------------------------------------------------- conveniences --------

@@ -199,3 +199,33 @@ def lowrank_bwd(x, z, U, dy, H, W, residual):
 __all__ = ["headwise_fwd", "headwise_bwd", "lowrank_filters", "lowrank_fwd",
            "lowrank_bwd_rows", "lowrank_dU", "lowrank_bwd", "num_threads",
            "set_num_threads", "LIB", "build_oracle"]
+
+
+# ------------------------------------------------------------ decode step ----
+# One new token per sequence with a carried state of the last W-1 inputs
+# (state[b, j] = x at time t-1-j; zeros before the sequence start).  The
+# pages leave inference to future engineering; the plainest reading is the
+# forward definition evaluated at the one new position, with the state as
+# its history.  Written here as exactly that: the W-token window [state
+# reversed, x_t] run through the full-sequence oracle, whose last row is y_t.
+
+def headwise_decode(x_t, w_t, state, H, residual):
+    """(y_t [B, C], new_state [B, W-1, C]) in fp64.  x_t [B, C], w_t [B, G, W],
+    state [B, W-1, C]."""
+    B, C = x_t.shape
+    W = w_t.shape[-1]
+    xs = x_t.double().cpu().reshape(B, 1, C)
+    st = state.double().cpu().reshape(B, W - 1, C)
+    window = torch.cat([st.flip(1), xs], dim=1)                  # times t-W+1 .. t
+    wwin = torch.zeros(B, W, w_t.shape[1], W, dtype=torch.float64)
+    wwin[:, W - 1] = w_t.double().cpu()
+    y = headwise_fwd(window, wwin, H, residual).reshape(B, W, C)[:, W - 1]
+    new_state = torch.cat([xs, st[:, :W - 2]], dim=1) if W > 1 else st
+    return y, new_state
+
+
+def lowrank_decode(x_t, z_t, U, state, H, W, residual):
+    """The low-rank decode step: filters z_t U, then the head-wise step."""
+    B, C = x_t.shape
+    w_t = lowrank_filters(z_t.reshape(B, 1, -1), U, C, H, W).reshape(B, C // H, W)
+    return headwise_decode(x_t, w_t, state, H, residual)
