@@ -16,6 +16,10 @@ Under torchrun each rank runs the full workload on its own GPU (independent
 replicas; no data-path collective), the timing is max over ranks, and the
 value is the bytes of all ranks over that time.
 
+--compare-static adds a second JSON line: per-call latency of the static
+short convolution (w [C, W]) next to head-wise DSC at H=1 and H=16, same
+shape, same GPU.
+
 --impl reference times the fp64 CPU oracle on the host cores instead, each
 step a bounded sample (the first 128 tokens of one sequence) of the same
 workload; it prints the same JSON line with "impl": "reference".
@@ -406,7 +410,52 @@ def run_dsc(args):
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob)
     print(json.dumps(line), flush=True)
+    if args.compare_static:
+        print(json.dumps(run_compare_static(dev, min(args.steps, 100))), flush=True)
     return 0
+
+
+def run_compare_static(dev, steps):
+    """Latency of the static short convolution (one filter per channel) next
+    to the dynamic ones at the bench shape: the comparison the pages draw
+    between DSC kernels and static short-conv kernels (their Figure 1), with
+    both sides built here and run on the same GPU."""
+    B, T, C, W = 8, 2048, 6144, 4
+    dt = torch.bfloat16
+    x = syn.draw((B, T, C), 1.0, 3, syn.SLOT_X, dt, dev)
+    dy = syn.draw((B, T, C), 1.0, 3, syn.SLOT_DY, dt, dev)
+    w = syn.static_filters(C, W, 0.5, 3, dt, dev)
+    y, dx, dw = torch.empty_like(x), torch.empty_like(x), torch.empty_like(w)
+    ws = torch.empty(max(dsc.dsc_static_bwd_workspace_size(B, T, C, W, dt), 16),
+                     dtype=torch.uint8, device=dev)
+    w1 = syn.draw((B, T, C, W), 0.5, 3, syn.SLOT_W, dt, dev)
+    dw1 = torch.empty_like(w1)
+    w16 = syn.draw((B, T, C // 16, W), 0.5, 4, syn.SLOT_W, dt, dev)
+    dw16 = torch.empty_like(w16)
+    cases = [
+        ("static_fwd", lambda: dsc.dsc_static_fwd(x, w, y, True)),
+        ("static_bwd", lambda: dsc.dsc_static_bwd(x, w, dy, dx, dw, ws, True)),
+        ("headwise_H1_fwd", lambda: dsc.dsc_headwise_fwd(x, w1, y, 1, True)),
+        ("headwise_H1_bwd", lambda: dsc.dsc_headwise_bwd(x, w1, dy, dx, dw1, 1, True)),
+        ("headwise_H16_fwd", lambda: dsc.dsc_headwise_fwd(x, w16, y, 16, True)),
+        ("headwise_H16_bwd", lambda: dsc.dsc_headwise_bwd(x, w16, dy, dx, dw16, 16, True)),
+    ]
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, f in cases:
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            f()
+        e.record(stream)
+        torch.cuda.synchronize()
+        out[name] = round(s.elapsed_time(e) / steps * 1e3, 2)
+    return {"comparison": "static_vs_dynamic_short_conv", "unit": "us_per_call",
+            "config": {"B": B, "T": T, "C": C, "W": W, "dtype": "bf16", "residual": True},
+            "us": out}
 
 
 def run_e2e(prob, calls, steps):
@@ -449,6 +498,8 @@ def main():
     ap.add_argument("--impl", default="dsc", choices=["dsc", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compare-static", action="store_true",
+                    help="also print a second line: static short conv vs DSC latency")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -136,6 +136,45 @@ dsc_status_t dsc_lowrank_bwd(const void* x, const void* z, const void* U,
                              dsc_dtype_t dtype, void* stream);
 
 /*
+ * Static short convolution: the special case of DSC whose filters do not
+ * depend on the token ("Dynamic Short Convolutions: The 'Locality Bias'
+ * Transformers Were Missing", Methodology: Adaptive Filtering at Scale,
+ * 1. Mathematical Intuition, the standard convolution; the static kernels of
+ * its Figure 1 compute the same operation).  One filter per channel:
+ *   y[b,t,c] = residual*x[b,t,c] + sum_{k=0}^{W-1} w[c,k] x[b,t-k,c]
+ * with x = 0 before t = 0 of each sequence (k = 0 is the current token).
+ *   x, y : [B, T, C]     w : [C, W]
+ * Equal to dsc_headwise_fwd with H = 1 and w broadcast over b and t.
+ * Arithmetic fp32, y rounded once.  Shape, alignment and aliasing rules as
+ * for dsc_headwise_fwd; B*T = 0 is a no-op.
+ */
+dsc_status_t dsc_static_fwd(const void* x, const void* w, void* y, int64_t B,
+                            int64_t T, int64_t C, int64_t W, int residual,
+                            dsc_dtype_t dtype, void* stream);
+
+/* Bytes of device workspace dsc_static_bwd needs for this shape (a function
+ * of the shape only); 0 for an invalid shape or B*T = 0. */
+size_t dsc_static_bwd_workspace_size(int64_t B, int64_t T, int64_t C,
+                                     int64_t W, dsc_dtype_t dtype);
+
+/*
+ * Backward of dsc_static_fwd:
+ *   dx[b,s,c] = residual*dy[b,s,c] + sum_{k: s+k<T} w[c,k] dy[b,s+k,c]
+ *   dw[c,k]   = sum_{b,t>=k} dy[b,t,c] x[b,t-k,c]      (over every token)
+ * dw is accumulated in fp32 (one partial per token range in the workspace,
+ * then added in a fixed order: bitwise reproducible) and rounded once.
+ * workspace: caller-owned device memory of at least
+ * dsc_static_bwd_workspace_size(...) bytes, 16-byte aligned, clobbered.
+ * B*T = 0 writes zeros to dw and touches nothing else (x, w, dy, dx and the
+ * workspace may then be NULL).
+ */
+dsc_status_t dsc_static_bwd(const void* x, const void* w, const void* dy,
+                            void* dx, void* dw, void* workspace,
+                            size_t workspace_bytes, int64_t B, int64_t T,
+                            int64_t C, int64_t W, int residual,
+                            dsc_dtype_t dtype, void* stream);
+
+/*
  * Decode step (inference, one new token per sequence) with a carried state.
  * The pages leave inference to future engineering; this is the forward
  * definition evaluated at one new position t with the last W-1 inputs of

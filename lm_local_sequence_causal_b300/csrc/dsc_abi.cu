@@ -173,6 +173,46 @@ dsc_status_t dsc_lowrank_decode(const void* x, const void* z, const void* U, voi
                                        (cudaStream_t)stream));
 }
 
+dsc_status_t dsc_static_fwd(const void* x, const void* w, void* y, int64_t B, int64_t T,
+                            int64_t C, int64_t W, int residual, dsc_dtype_t dtype,
+                            void* stream) {
+  dsc_status_t st = check_shape(B, T, C, 1, W, 0, dtype, false);
+  if (st != DSC_OK) return st;
+  if (B * T == 0) return DSC_OK;
+  if ((st = check_ptrs({x, w, y})) != DSC_OK) return st;
+  if (x == y) return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::static_fwd(x, w, y, make_shape(B, T, C, 1, W, 0, residual, dtype),
+                                   (cudaStream_t)stream));
+}
+
+size_t dsc_static_bwd_workspace_size(int64_t B, int64_t T, int64_t C, int64_t W,
+                                     dsc_dtype_t dtype) {
+  if (check_shape(B, T, C, 1, W, 0, dtype, false) != DSC_OK || B * T == 0) return 0;
+  return dsc::static_bwd_workspace(make_shape(B, T, C, 1, W, 0, 0, dtype));
+}
+
+dsc_status_t dsc_static_bwd(const void* x, const void* w, const void* dy, void* dx, void* dw,
+                            void* workspace, size_t workspace_bytes, int64_t B, int64_t T,
+                            int64_t C, int64_t W, int residual, dsc_dtype_t dtype,
+                            void* stream) {
+  dsc_status_t st = check_shape(B, T, C, 1, W, 0, dtype, false);
+  if (st != DSC_OK) return st;
+  if (B * T == 0) {
+    // dw is a sum over zero tokens: all zeros.  Nothing else to write.
+    if (dw == nullptr) return DSC_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)C * W * (dtype == DSC_BF16 ? 2 : 4);
+    return from_cuda(cudaMemsetAsync(dw, 0, bytes, (cudaStream_t)stream));
+  }
+  if ((st = check_ptrs({x, w, dy, dx, dw})) != DSC_OK) return st;
+  if (dx == x || dx == dy || dx == dw || dw == x || dw == w || dw == dy)
+    return DSC_ERR_INVALID_ARG;
+  const Shape s = make_shape(B, T, C, 1, W, 0, residual, dtype);
+  const size_t need = dsc::static_bwd_workspace(s);
+  if (workspace == nullptr || workspace_bytes < need) return DSC_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return DSC_ERR_ALIGNMENT;
+  return from_cuda(dsc::static_bwd(x, w, dy, dx, dw, workspace, s, (cudaStream_t)stream));
+}
+
 int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
                                   int64_t R, dsc_dtype_t dtype) {
   if (check_shape(B, T, C, H, W, R, dtype, true) != DSC_OK) return -1;

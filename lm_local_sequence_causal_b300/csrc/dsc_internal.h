@@ -41,6 +41,13 @@ cudaError_t headwise_decode(const void* x, const void* w, void* state, void* y, 
 cudaError_t lowrank_decode(const void* x, const void* z, const void* U, void* state, void* y,
                            const Shape& s, cudaStream_t st);
 
+// Static short convolution, filters w [C, W] constant over t (static_conv.cu).
+// H = 1.  The backward needs a caller-owned fp32 workspace for the dw partials.
+cudaError_t static_fwd(const void* x, const void* w, void* y, const Shape& s, cudaStream_t st);
+size_t static_bwd_workspace(const Shape& s);
+cudaError_t static_bwd(const void* x, const void* w, const void* dy, void* dx, void* dw,
+                       void* ws, const Shape& s, cudaStream_t st);
+
 // Low-rank kernels (lowrank_simt.cu).
 bool lowrank_supported(const Shape& s);
 cudaError_t lowrank_fwd(const void* x, const void* z, const void* U, void* y,
@@ -75,6 +82,10 @@ bool make_tmap_3d(CUtensorMap* tm, const void* base, bool bf16, uint64_t d0, uin
 bool make_tmap_4d_bf16(CUtensorMap* tm, const void* base, const uint64_t dims[4],
                        const uint64_t strides_bytes[3], const uint32_t box[4]);
 int sm_count();
+// Token ranges for a streaming grid of `ncb` channel blocks: as many CTAs as
+// fit on the GPU at once (occupancy of `kernel` x SMs), at least 16 tokens
+// each.
+int64_t n_ranges(const void* kernel, int threads, int64_t ncb, int64_t N);
 
 // Opt in to large dynamic shared memory, once per kernel and device.  The
 // template parameter `Tag` keeps one record per kernel instance (all

@@ -344,40 +344,6 @@ __global__ void hw_dw_generic(const T* __restrict__ x, const T* __restrict__ dy,
 
 // ------------------------------------------------------------ dispatch ----
 
-// Token ranges for a grid of `ncb` channel blocks: as many CTAs as fit on
-// the GPU at once (occupancy of this kernel x SMs), at least 16 tokens each.
-// Resident CTAs per SM of `kernel` at `threads` threads, cached per kernel
-// (keyed by its address: every instance of one template shares a type).
-int blocks_per_sm(const void* kernel, int threads) {
-  static std::mutex mu;
-  static const void* keys[64] = {};
-  static int vals[64] = {};
-  std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < 64; ++i) {
-    if (keys[i] == kernel) return vals[i];
-    if (keys[i] == nullptr) {
-      int nb = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess ||
-          nb <= 0)
-        nb = 2;
-      keys[i] = kernel;
-      vals[i] = nb;
-      return nb;
-    }
-  }
-  return 2;
-}
-
-// Token ranges for a grid of `ncb` channel blocks: as many CTAs as fit on
-// the GPU at once (occupancy of this kernel x SMs), at least 16 tokens each.
-int64_t n_ranges(const void* kernel, int threads, int64_t ncb, int64_t N) {
-  const int per_sm = blocks_per_sm(kernel, threads);
-  const int sms = sm_count() > 0 ? sm_count() : 148;
-  int64_t r = std::max<int64_t>(1, static_cast<int64_t>(per_sm) * sms / ncb);
-  r = std::min<int64_t>(r, std::max<int64_t>(1, N / 16));
-  return std::min<int64_t>(r, (int64_t(1) << 31) / ncb - 1);
-}
-
 template <typename T>
 int ng_of(int64_t H) {
   constexpr int V = Vec<T>::N;

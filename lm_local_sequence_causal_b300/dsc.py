@@ -55,6 +55,12 @@ def load():
     lib.dsc_headwise_decode.argtypes = [P, P, P, P, I64, I64, I64, I64, INT, INT, P]
     lib.dsc_lowrank_decode.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, INT, INT, P]
     lib.dsc_headwise_decode.restype = INT
+    lib.dsc_static_fwd.argtypes = [P, P, P, I64, I64, I64, I64, INT, INT, P]
+    lib.dsc_static_fwd.restype = INT
+    lib.dsc_static_bwd_workspace_size.argtypes = [I64, I64, I64, I64, INT]
+    lib.dsc_static_bwd_workspace_size.restype = SZ
+    lib.dsc_static_bwd.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64, INT, INT, P]
+    lib.dsc_static_bwd.restype = INT
     lib.dsc_lowrank_decode.restype = INT
     lib.dsc_lowrank_uses_tensor_cores.argtypes = [I64, I64, I64, I64, I64, I64, INT]
     lib.dsc_lowrank_uses_tensor_cores.restype = INT
@@ -210,6 +216,33 @@ def dsc_lowrank_decode(x, z, U, state, y, H, W, residual=True, stream=None):
                                      _dtype_code(x), _stream(stream)), "dsc_lowrank_decode")
 
 
+def dsc_static_fwd(x, w, y, residual=True, stream=None):
+    """Static short conv: y[b,t,c] = residual*x + sum_k w[c,k] x[b,t-k,c]; w is [C, W]."""
+    B, T, C = _bt_c(x)
+    W = w.shape[-1]
+    dt = x.dtype
+    _check(load().dsc_static_fwd(_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(y, dt, "y"),
+                                 B, T, C, W, int(bool(residual)), _dtype_code(x),
+                                 _stream(stream)), "dsc_static_fwd")
+
+
+def dsc_static_bwd_workspace_size(B, T, C, W, dtype) -> int:
+    return int(load().dsc_static_bwd_workspace_size(B, T, C, W, _DTYPES[dtype]))
+
+
+def dsc_static_bwd(x, w, dy, dx, dw, workspace, residual=True, stream=None):
+    """dx [B,T,C] and dw [C,W] of the static short conv; `workspace` is a uint8 CUDA tensor."""
+    B, T, C = _bt_c(x)
+    W = w.shape[-1]
+    dt = x.dtype
+    ws_ptr = _ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(load().dsc_static_bwd(_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(dy, dt, "dy"),
+                                 _ptr(dx, dt, "dx"), _ptr(dw, dt, "dw"), ws_ptr, ws_bytes,
+                                 B, T, C, W, int(bool(residual)), _dtype_code(x),
+                                 _stream(stream)), "dsc_static_bwd")
+
+
 # ------------------------------------------------------- conveniences --------
 
 def headwise_fwd(x, w, H, residual=True):
@@ -245,3 +278,20 @@ def lowrank_bwd(x, z, U, dy, H, W, residual=True, workspace=None):
         workspace = lowrank_workspace(x, z, H, W)
     dsc_lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, H, W, residual)
     return dx, dz, dU
+
+
+def static_fwd(x, w, residual=True):
+    y = torch.empty_like(x)
+    dsc_static_fwd(x, w, y, residual)
+    return y
+
+
+def static_bwd(x, w, dy, residual=True, workspace=None):
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(w)
+    if workspace is None:
+        B, T, C = x.shape
+        n = dsc_static_bwd_workspace_size(B, T, C, w.shape[-1], x.dtype)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=x.device)
+    dsc_static_bwd(x, w, dy, dx, dw, workspace, residual)
+    return dx, dw

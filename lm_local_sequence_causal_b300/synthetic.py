@@ -20,6 +20,8 @@ deviation a):
   qkv_lowrank     same x; R=16, H=1; z and U std 1/sqrt(R).
   all-linear sweep C in {2048, 6144, 5632} x T in {512, 2048, 8192} with
                   B = 16384 / T, W in {2, 3, 4}; head-wise H=16, low-rank R=16.
+  static conv     the head-wise shapes with H=1 and one filter per channel,
+                  w [C, W] std 0.5 (``static_filters``).
   linear_rnn      B=2 T=16384 C=4096 W=4; head-wise H=64, low-rank R=16;
                   x ~ N(0,1) with round(0.05 C) channels (a seeded random
                   choice) scaled by 8 to stress accumulation.
@@ -145,6 +147,11 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu", need_grad_inputs=True
     if need_grad_inputs:
         out["dy"] = draw((B, T, C), 1.0, seed, SLOT_DY, wl.dtype, device)
     return out
+
+
+def static_filters(C: int, W: int, std: float, seed: int, dtype, device="cpu"):
+    """Filters w [C, W] of the static short convolution (one per channel)."""
+    return draw((C, W), std, seed, SLOT_W, dtype, device)
 
 
 def sample_rows(B: int, T: int, W: int, n: int, seed: int = 0, tile: int = 64):

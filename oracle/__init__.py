@@ -229,3 +229,64 @@ def lowrank_decode(x_t, z_t, U, state, H, W, residual):
     B, C = x_t.shape
     w_t = lowrank_filters(z_t.reshape(B, 1, -1), U, C, H, W).reshape(B, C // H, W)
     return headwise_decode(x_t, w_t, state, H, residual)
+
+
+# -------------------------------------------------- static short conv ------
+# "Dynamic Short Convolutions: The 'Locality Bias' Transformers Were
+# Missing", Methodology: Adaptive Filtering at Scale, 1. Mathematical
+# Intuition: the standard (static) convolution has one filter per channel,
+# the same at every token.  It is the head-wise definition with H = 1 and
+# w[b,t] = w for all b, t; its filter gradient is the head-wise dw summed
+# over every token.  Written here as exactly that composition.
+
+def _broadcast_w(w, B, T):
+    C, W = w.shape
+    return w.double().cpu().reshape(1, 1, C, W).expand(B, T, C, W).contiguous()
+
+
+def static_fwd(x, w, residual, rows=None):
+    """y of the static short conv, w [C, W]; full or for the listed rows.
+
+    For rows, each listed token is evaluated on its own W-token causal
+    window (zeros before the sequence start, as the definition pads)."""
+    B, T, C = x.shape
+    W = w.shape[-1]
+    if rows is None:
+        return headwise_fwd(x, _broadcast_w(w, B, T), 1, residual)
+    rows = rows.to(torch.int64).cpu()
+    xd = x.double().cpu().reshape(B * T, C)
+    n = rows.numel()
+    win = torch.zeros(n, W, C, dtype=torch.float64)
+    t = rows % T
+    for j in range(W):                      # window slot j holds time t-(W-1)+j
+        back = W - 1 - j
+        ok = t >= back
+        win[ok, j] = xd[rows[ok] - back]
+    return headwise_fwd(win, _broadcast_w(w, n, W), 1, residual)[:, W - 1]
+
+
+def static_bwd(x, w, dy, residual):
+    """(dx [B,T,C], dw [C,W]) of the static short conv over the whole batch."""
+    B, T, C = x.shape
+    dx, dw_tok = headwise_bwd(x, _broadcast_w(w, B, T), dy, 1, residual)
+    return dx, dw_tok.sum(dim=(0, 1)).reshape(C, -1)
+
+
+def static_dx_rows(w, dy, residual, T, rows):
+    """dx of the static short conv for the listed token rows (dy [B,T,C]).
+
+    dx at time s depends on dy at s..s+W-1 of the same sequence only; each
+    row is evaluated on that forward window (zeros past the sequence end)."""
+    B, _, C = dy.shape
+    W = w.shape[-1]
+    rows = rows.to(torch.int64).cpu()
+    gd = dy.double().cpu().reshape(B * T, C)
+    n = rows.numel()
+    win = torch.zeros(n, W, C, dtype=torch.float64)
+    s = rows % T
+    for j in range(W):                      # window slot j holds time s+j
+        ok = s + j < T
+        win[ok, j] = gd[rows[ok] + j]
+    dx, _ = headwise_bwd(torch.zeros(n, W, C, dtype=torch.float64), _broadcast_w(w, n, W),
+                         win, 1, residual)
+    return dx[:, 0]

@@ -137,3 +137,28 @@ def test_lowrank_path_query():
     assert q(8, 2048, 6144, 1, 4, 0, bf) == -1
     assert q(8, 2048, 6144, 1, 5, 16, bf) == -1
     assert q(8, 2048, 6144, 3, 4, 16, bf) == -1
+
+
+def test_static_validation_and_workspace(lib):
+    f = lib.dsc_static_fwd
+    assert f(A, A2, A3, 2, 8, 60, 4, 1, BF16, None) == dsc.DSC_ERR_ALIGNMENT   # C % 8
+    assert f(A, A2, A3, 2, 8, 64, 5, 1, BF16, None) == dsc.DSC_ERR_UNSUPPORTED  # W > 4
+    assert f(A, A2, A, 2, 8, 64, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG   # y aliases x
+    assert f(A, MIS, A3, 2, 8, 64, 4, 1, BF16, None) == dsc.DSC_ERR_ALIGNMENT
+    assert f(None, None, None, 0, 8, 64, 4, 1, BF16, None) == dsc.DSC_OK       # empty
+    ws = lib.dsc_static_bwd_workspace_size
+    n = ws(8, 2048, 6144, 4, BF16)
+    # one fp32 partial per token range, channel and tap; a function of the shape only
+    assert n > 0 and n % (6144 * 4 * 4) == 0 and n == ws(8, 2048, 6144, 4, BF16)
+    assert ws(0, 2048, 6144, 4, BF16) == 0
+    assert ws(8, 2048, 6144, 5, BF16) == 0
+    g = lib.dsc_static_bwd
+    assert g(A, A2, A3, A4, A5, None, 0, 8, 2048, 6144, 4, 1, BF16, None) == dsc.DSC_ERR_WORKSPACE
+    assert g(A, A2, A3, A4, A5, P(0x60000), n - 16, 8, 2048, 6144, 4, 1, BF16,
+             None) == dsc.DSC_ERR_WORKSPACE
+    assert g(A, A2, A3, A4, A5, P(0x60008), n, 8, 2048, 6144, 4, 1, BF16,
+             None) == dsc.DSC_ERR_ALIGNMENT
+    assert g(A, A2, A3, A, A5, P(0x60000), n, 8, 2048, 6144, 4, 1, BF16,
+             None) == dsc.DSC_ERR_INVALID_ARG                                   # dx aliases x
+    assert g(A, A2, A3, A4, None, None, 0, 0, 8, 64, 4, 1, BF16,
+             None) == dsc.DSC_ERR_INVALID_ARG                                   # empty, no dw
