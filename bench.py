@@ -500,11 +500,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--compare-static", action="store_true",
                     help="also print a second line: static short conv vs DSC latency")
+    ap.add_argument("--compare-static-only", action="store_true",
+                    help="print only the static-vs-DSC latency line (single GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.compare_static_only:
+        torch.cuda.set_device(0)
+        dsc.load()
+        print(json.dumps(run_compare_static(torch.device("cuda", 0), min(args.steps, 100))),
+              flush=True)
+        return 0
     return run_dsc(args)
 
 

@@ -360,17 +360,20 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 // dw tiles one tap pair at a time; at chunk ends it reads out the dU
 // accumulator, at the end the dz ones).  The two groups run independently.
 
-template <int W>
+// RK = K-steps of 16 ranks (R padded to 16 * RK with zeros).
+template <int W, int RK>
 struct BwdLayout {
+  static constexpr int RP = 16 * RK;                      // padded rank
   static constexpr int NT = W <= 2 ? 2 : 4;               // dw taps incl. zero padding
   static constexpr int XROWS = BM + W - 1;
   static constexpr int XBOX = XROWS * 128;
   static constexpr int XBYTES = round1k(XBOX);
-  static constexpr int ZBOX = XROWS * 32;                 // [2 halves][XROWS][16 B]
+  static constexpr int ZBOX = XROWS * 2 * RP;             // [RP/8 groups][XROWS][16 B]
   static constexpr int ZBYTES = round1k(ZBOX);
-  static constexpr int NSTB = 3;
+  static constexpr int NSTB = RK == 1 ? 3 : 2;
   static constexpr int STAGE = 2 * XBYTES + ZBYTES;       // x, dy, z
-  static constexpr int UBYTES = W * 2048;                 // U tiles of one chunk
+  static constexpr int UTAP = 2048 * RK;                  // U tile of one tap: [RP r][64 c]
+  static constexpr int UBYTES = W * UTAP;                 // U tiles of one chunk
   static constexpr int UALLOC = round1k(UBYTES);
   static constexpr int DWTAP = BM * 128;                  // one tap of dw (16 KB)
   static constexpr int STG_OFF = 0;
@@ -385,26 +388,27 @@ struct BwdLayout {
   static constexpr int TOTAL = MISC_OFF + 16 + 1024;
   static constexpr uint32_t TX = 2 * XBOX + ZBOX;
   static constexpr int TM_D = 0;                          // W x 64 columns
-  static constexpr int TM_DU = W * 64;                    // 2 buffers x NT/2 x 16
-  static constexpr int TM_DZ = TM_DU + NT * 16;           // 16 per tile of the split
-  static constexpr int TPS_MAX = (512 - TM_DZ) / 16;
+  static constexpr int TM_DU = W * 64;                    // 2 buffers x NT/2 x RP
+  static constexpr int TM_DZ = TM_DU + NT * RP;           // RP per tile of the split
+  static constexpr int TPS_MAX = (512 - TM_DZ) / RP;
 };
 
 struct BwdArgs {
   __nv_bfloat16* dx;       // [B][T][C]
-  float* dz_part;          // [S][B*T][16]
-  float* dU_part;          // [P][16][C*W]
-  const unsigned char* uimg;  // [nchunks][W][16 rows][128 B] swizzled U tiles
+  float* dz_part;          // [S][B*T][RP]
+  float* dU_part;          // [P][RP][C*W]
+  const unsigned char* uimg;  // [nchunks][W][RP rows][128 B] swizzled U tiles
   int T, C, ntiles, nchunks, S, P, ntl, residual;
 };
 
-template <int W>
+template <int W, int RK>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
           const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dx,
           const BwdArgs args) {
-  using L = BwdLayout<W>;
+  using L = BwdLayout<W, RK>;
   constexpr int NST_ = L::NSTB;
+  constexpr int RP = L::RP;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1k(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -541,8 +545,11 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const uint32_t ut = sb + L::U_OFF + (lc & 1) * L::UALLOC;
 #pragma unroll
         for (int k = 0; k < W; ++k)
-          mma_bf16(tmem + L::TM_D + k * 64, make_desc(zt + 16 * k, zsbo, 128, 0),
-                   make_desc(ut + k * 2048, 16, 1024, 2), id_d, 0u);
+#pragma unroll
+          for (int ks = 0; ks < RK; ++ks)
+            mma_bf16(tmem + L::TM_D + k * 64, make_desc(zt + 16 * k + 2 * ks * zsbo, zsbo, 128, 0),
+                     make_desc(ut + k * L::UTAP + ks * 2048, 16, 1024, 2), id_d,
+                     ks > 0 ? 1u : 0u);
         mma_commit(bar_dfull);
         mma_commit(bar_empty + 8 * s);
         if (lt == ntile - 1) mma_commit(bar_ufree + 8 * (lc & 1));
@@ -555,8 +562,8 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     // dz and dU for every item, one tap pair at a time as the dw group
     // finishes writing it.
     if (lane == 0) {
-      constexpr uint32_t id_dz = idesc_major(BM, 16, 0, 0);   // A dw K-major, B U K-major
-      constexpr uint32_t id_du = idesc_major(BM, 16, 1, 1);   // A dw^T MN-major, B z MN-major
+      constexpr uint32_t id_dz = idesc_major(BM, RP, 0, 0);   // A dw K-major, B U K-major
+      constexpr uint32_t id_du = idesc_major(BM, RP, 1, 1);   // A dw^T MN-major, B z MN-major
       const uint32_t zsbo = L::XROWS * 16;
       bool ok = true;
       int issued_pair[2] = {0, 0};
@@ -589,11 +596,11 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             const int q = 8 * pr + i;
             const int k = q >> 2, cb = q & 3;
             if (k < W)
-              mma_bf16(tmem + L::TM_DZ + lt * 16,
+              mma_bf16(tmem + L::TM_DZ + lt * RP,
                        make_desc(dw + k * L::DWTAP + cb * 32, 16, 1024, 2),
-                       make_desc(ut + k * 2048 + cb * 32, 16, 1024, 2), id_dz,
+                       make_desc(ut + k * L::UTAP + cb * 32, 16, 1024, 2), id_dz,
                        (lc > 0 || q > 0) ? 1u : 0u);
-            mma_bf16(tmem + L::TM_DU + ub * (L::NT / 2) * 16 + pr * 16,
+            mma_bf16(tmem + L::TM_DU + ub * (L::NT / 2) * RP + pr * RP,
                      make_desc(dw + 2 * pr * L::DWTAP + i * 2048, L::DWTAP, 1024, 2),
                      make_desc(zt + i * 256, 128, zsbo, 0), id_du,
                      (lt > 0 || i > 0) ? 1u : 0u);
@@ -744,17 +751,20 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
           if (!__all_sync(0xffffffffu, ok)) break;
           tc_fence_after();
           if (h < L::NT / 2) {
-            uint32_t v[16];
-            tmem_ld16(tmem + tlane + L::TM_DU + ub * (L::NT / 2) * 16 + h * 16, v);
+            uint32_t v[RP];
+#pragma unroll
+            for (int ks = 0; ks < RK; ++ks)
+              tmem_ld16(tmem + tlane + L::TM_DU + ub * (L::NT / 2) * RP + h * RP + 16 * ks,
+                        v + 16 * ks);
             tmem_wait_ld();
-            tmem_regs_ready<16>(v);
+            tmem_regs_ready<RP>(v);
             const int jp = h * 128 + tl;                  // tap-major column of the chunk
             const int k = jp >> 6, c = c0 + (jp & 63);
             if (k < W && c < args.C) {
-              float* dst = args.dU_part + static_cast<size_t>(split) * 16 * CW +
+              float* dst = args.dU_part + static_cast<size_t>(split) * RP * CW +
                            static_cast<int64_t>(c) * W + k;
 #pragma unroll
-              for (int r = 0; r < 16; ++r)
+              for (int r = 0; r < RP; ++r)
                 dst[static_cast<int64_t>(r) * CW] = __uint_as_float(v[r]);
             }
           }
@@ -769,18 +779,20 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         if (__all_sync(0xffffffffu, ok)) {
           tc_fence_after();
           for (int lt = h; lt < ntile; lt += 2) {
-            uint32_t v[16];
-            tmem_ld16(tmem + tlane + L::TM_DZ + lt * 16, v);
+            uint32_t v[RP];
+#pragma unroll
+            for (int ks = 0; ks < RK; ++ks)
+              tmem_ld16(tmem + tlane + L::TM_DZ + lt * RP + 16 * ks, v + 16 * ks);
             tmem_wait_ld();
-            tmem_regs_ready<16>(v);
+            tmem_regs_ready<RP>(v);
             const int gt = tl0 + lt;
             const int b = gt / args.ntiles, t = (gt - b * args.ntiles) * BM + tl;
             if (t < args.T) {
               float4* dst = reinterpret_cast<float4*>(
                   args.dz_part + (static_cast<size_t>(slice) * Ntok +
-                                  static_cast<int64_t>(b) * args.T + t) * 16);
+                                  static_cast<int64_t>(b) * args.T + t) * RP);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
+              for (int i = 0; i < RP / 4; ++i)
                 dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
             }
@@ -800,15 +812,17 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 }
 
 // U rearranged into the shared-memory image of the backward's U tiles: for
-// chunk ch and tap k, a [16 r][64 c] tile with 128-byte rows and the TMA
-// 128-byte swizzle, element (r, c) = U[r, (64*ch + c)*W + k] (zero past C).
-template <int W>
+// chunk ch and tap k, a [RP r][64 c] tile with 128-byte rows and the TMA
+// 128-byte swizzle, element (r, c) = U[r, (64*ch + c)*W + k] (zero past C
+// and for the padding ranks r >= R).
+template <int W, int RK>
 __global__ void lr_u_image(const __nv_bfloat16* __restrict__ U, unsigned char* __restrict__ img,
-                           int C, int nchunks) {
+                           int C, int R, int nchunks) {
+  constexpr int RP = 16 * RK;
   const int64_t CW = static_cast<int64_t>(C) * W;
-  const int total = nchunks * W * 16 * 8;              // 16-byte pieces
+  const int total = nchunks * W * RP * 8;              // 16-byte pieces
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-    const int piece = i & 7, r = (i >> 3) & 15, tile = i >> 7;
+    const int piece = i & 7, r = (i >> 3) % RP, tile = (i >> 3) / RP;
     const int k = tile % W, ch = tile / W;
     uint32_t w4[4];
 #pragma unroll
@@ -818,22 +832,24 @@ __global__ void lr_u_image(const __nv_bfloat16* __restrict__ U, unsigned char* _
       for (int hh = 0; hh < 2; ++hh) {
         const int c = ch * CC + piece * 8 + 2 * e + hh;
         uint32_t bits = 0;
-        if (c < C) bits = __bfloat16_as_ushort(U[static_cast<int64_t>(r) * CW + static_cast<int64_t>(c) * W + k]);
+        if (c < C && r < R)
+          bits = __bfloat16_as_ushort(U[static_cast<int64_t>(r) * CW + static_cast<int64_t>(c) * W + k]);
         pair |= bits << (16 * hh);
       }
       w4[e] = pair;
     }
     const uint32_t off = static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(piece) ^ (r & 7u)) << 4);
-    *reinterpret_cast<uint4*>(img + static_cast<size_t>(tile) * 2048 + off) =
+    *reinterpret_cast<uint4*>(img + static_cast<size_t>(tile) * (2048 * RK) + off) =
         make_uint4(w4[0], w4[1], w4[2], w4[3]);
   }
 }
 
 // dz[n, r] = sum_s dz_part[s][n][r]; dU[r, j] = sum_p dU_part[p][r][j]; fixed
-// order, fp32, rounded once to bf16.  Four outputs per thread.
+// order, fp32, rounded once to bf16.  Four outputs per thread.  The partials
+// hold RP >= R ranks (R a multiple of 8); the padding ranks are skipped.
 __global__ void lr_reduce_tc(const float* __restrict__ dz_part, const float* __restrict__ dU_part,
                              __nv_bfloat16* __restrict__ dz, __nv_bfloat16* __restrict__ dU,
-                             int64_t nz4, int S, int64_t nU4, int P) {
+                             int64_t nz4, int S, int64_t nU4, int P, int R, int RP, int64_t CW) {
   const int64_t total = nz4 + nU4;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -843,15 +859,20 @@ __global__ void lr_reduce_tc(const float* __restrict__ dz_part, const float* __r
     __nv_bfloat16* out;
     int64_t j;
     if (i < nz4) {
+      // i = n * RP/4 + r/4 in the partials; written at n * R + r
+      const int64_t n = i / (RP / 4);
+      const int r = static_cast<int>(i - n * (RP / 4)) * 4;
+      if (r >= R) continue;
       src = reinterpret_cast<const float4*>(dz_part) + i;
       stride = nz4;
       cnt = S;
       out = dz;
-      j = i;
+      j = (n * R + r) / 4;
     } else {
+      // the first R rows of each split's [RP][C*W] partial
       j = i - nz4;
       src = reinterpret_cast<const float4*>(dU_part) + j;
-      stride = nU4;
+      stride = static_cast<int64_t>(RP) * CW / 4;
       cnt = P;
       out = dU;
     }
@@ -906,12 +927,22 @@ struct TcBwdPlan {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-int tps_max(int64_t W) {
+int rk_of(int64_t R) { return R > 16 ? 2 : 1; }
+
+int tps_max(int64_t W, int RK) {
+  if (RK == 2) {
+    switch (W) {
+      case 1: return BwdLayout<1, 2>::TPS_MAX;
+      case 2: return BwdLayout<2, 2>::TPS_MAX;
+      case 3: return BwdLayout<3, 2>::TPS_MAX;
+      default: return BwdLayout<4, 2>::TPS_MAX;
+    }
+  }
   switch (W) {
-    case 1: return BwdLayout<1>::TPS_MAX;
-    case 2: return BwdLayout<2>::TPS_MAX;
-    case 3: return BwdLayout<3>::TPS_MAX;
-    default: return BwdLayout<4>::TPS_MAX;
+    case 1: return BwdLayout<1, 1>::TPS_MAX;
+    case 2: return BwdLayout<2, 1>::TPS_MAX;
+    case 3: return BwdLayout<3, 1>::TPS_MAX;
+    default: return BwdLayout<4, 1>::TPS_MAX;
   }
 }
 
@@ -924,7 +955,9 @@ TcBwdPlan plan_bwd_tc(const Shape& s, int nsm) {
   p.ntiles = static_cast<int>((s.T + BM - 1) / BM);
   p.nchunks = static_cast<int>((s.C + CC - 1) / CC);
   p.ntl = static_cast<int>(s.B * p.ntiles);
-  const int tmax = tps_max(s.W);
+  const int RK = rk_of(s.R);
+  const size_t RP = 16 * static_cast<size_t>(RK);
+  const int tmax = tps_max(s.W, RK);
   const double item = 3.0 * BM * CC * 2;
   const double N = static_cast<double>(s.B) * s.T, CW = static_cast<double>(s.C) * s.W;
   double best = -1;
@@ -943,21 +976,25 @@ TcBwdPlan plan_bwd_tc(const Shape& s, int nsm) {
     }
   }
   p.dz_off = 0;
-  p.dU_off = align_up(static_cast<size_t>(p.S) * s.B * s.T * 16 * sizeof(float), 256);
-  p.img_off = p.dU_off + align_up(static_cast<size_t>(p.P) * 16 * s.C * s.W * sizeof(float), 256);
-  p.total = p.img_off + align_up(static_cast<size_t>(p.nchunks) * s.W * 2048, 256);
+  p.dU_off = align_up(static_cast<size_t>(p.S) * s.B * s.T * RP * sizeof(float), 256);
+  p.img_off = p.dU_off + align_up(static_cast<size_t>(p.P) * RP * s.C * s.W * sizeof(float), 256);
+  p.total = p.img_off + align_up(static_cast<size_t>(p.nchunks) * s.W * 2048 * RK, 256);
   return p;
 }
 
-template <int W>
+template <int W, int RK>
 cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* dy, void* dx,
                        void* dz, void* dU, void* ws, const Shape& s, const TcBwdPlan& p,
                        cudaStream_t st) {
-  using L = BwdLayout<W>;
+  using L = BwdLayout<W, RK>;
   CUtensorMap tx, tdy, tz, tdx;
-  const uint64_t zd[4] = {8, static_cast<uint64_t>(s.T), 2, static_cast<uint64_t>(s.B)};
-  const uint64_t zs[3] = {16 * 2, 16, static_cast<uint64_t>(s.T) * 16 * 2};
-  const uint32_t zb[4] = {8, static_cast<uint32_t>(L::XROWS), 2, 1};
+  // z [B][T][R] seen as [B][R/8 groups][T][8]: group g of token t at byte
+  // offset t*2R + 16g.  The box covers RP/8 groups; groups past R/8 read as
+  // zero (the padding ranks).
+  const uint64_t R = static_cast<uint64_t>(s.R);
+  const uint64_t zd[4] = {8, static_cast<uint64_t>(s.T), R / 8, static_cast<uint64_t>(s.B)};
+  const uint64_t zs[3] = {R * 2, 16, static_cast<uint64_t>(s.T) * R * 2};
+  const uint32_t zb[4] = {8, static_cast<uint32_t>(L::XROWS), static_cast<uint32_t>(L::RP / 8), 1};
   if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
       !make_tmap_3d(&tdy, dy, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
       !make_tmap_3d(&tdx, dx, true, s.C, s.T, s.B, CC, BM, 128) ||
@@ -978,30 +1015,32 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
   a.ntl = p.ntl;
   a.residual = s.residual;
   {
-    const int pieces = p.nchunks * W * 128;
-    lr_u_image<W><<<std::min(1184, (pieces + 255) / 256), 256, 0, st>>>(
+    const int pieces = p.nchunks * W * L::RP * 8;
+    lr_u_image<W, RK><<<std::min(1184, (pieces + 255) / 256), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(U), base + p.img_off, static_cast<int>(s.C),
-        p.nchunks);
+        static_cast<int>(s.R), p.nchunks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto kern = lr_bwd_tc<W>;
+  static_assert(L::TOTAL <= 227 * 1024, "backward shared memory");
+  auto kern = lr_bwd_tc<W, RK>;
   cudaError_t e = set_smem<L>(kern, L::TOTAL);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(p.S * p.P), kBwdThreads, L::TOTAL, st>>>(tx, tdy, tz, tdx, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t nz4 = s.B * s.T * 16 / 4, nU4 = 16 * s.C * s.W / 4;
+  const int64_t nz4 = s.B * s.T * L::RP / 4, nU4 = s.R * s.C * s.W / 4;
   const int blocks = static_cast<int>(std::min<int64_t>((nz4 + nU4 + 255) / 256, 148 * 8));
   lr_reduce_tc<<<blocks, 256, 0, st>>>(a.dz_part, a.dU_part, static_cast<__nv_bfloat16*>(dz),
-                                       static_cast<__nv_bfloat16*>(dU), nz4, p.S, nU4, p.P);
+                                       static_cast<__nv_bfloat16*>(dU), nz4, p.S, nU4, p.P,
+                                       static_cast<int>(s.R), L::RP, s.C * s.W);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool lowrank_bwd_tc_supported(const Shape& s) {
-  return s.bf16 && s.H == 1 && s.R == 16 && s.W >= 1 && s.W <= 4 &&
+  return s.bf16 && s.H == 1 && s.R >= 8 && s.R <= 32 && s.R % 8 == 0 && s.W >= 1 && s.W <= 4 &&
          s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.T < (int64_t(1) << 30) &&
          s.C < (int64_t(1) << 24);
 }
@@ -1019,16 +1058,24 @@ cudaError_t lowrank_bwd_tc(const void* x, const void* z, const void* U, const vo
   const int nsm = sm_count();
   if (nsm <= 0) return cudaErrorNoDevice;
   const TcBwdPlan p = plan_bwd_tc(s, nsm);
+  if (rk_of(s.R) == 2) {
+    switch (s.W) {
+      case 1: return launch_bwd<1, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+      case 2: return launch_bwd<2, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+      case 3: return launch_bwd<3, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+      default: return launch_bwd<4, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+    }
+  }
   switch (s.W) {
-    case 1: return launch_bwd<1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-    case 2: return launch_bwd<2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-    case 3: return launch_bwd<3>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-    default: return launch_bwd<4>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+    case 1: return launch_bwd<1, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+    case 2: return launch_bwd<2, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+    case 3: return launch_bwd<3, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
+    default: return launch_bwd<4, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
   }
 }
 
 bool lowrank_tc_supported(const Shape& s) {
-  return s.bf16 && s.H == 1 && (s.R == 16 || s.R == 32) && s.W >= 1 && s.W <= 4 &&
+  return s.bf16 && s.H == 1 && s.R >= 8 && s.R <= 32 && s.R % 8 == 0 && s.W >= 1 && s.W <= 4 &&
          s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.T < (int64_t(1) << 30) &&
          s.C < (int64_t(1) << 24);
 }

@@ -128,11 +128,12 @@ def test_lowrank_path_query():
     assert q(8, 2048, 6144, 1, 4, 16, bf) == 3
     assert q(32, 512, 5632, 1, 3, 16, bf) == 3
     assert q(2, 16384, 4096, 1, 4, 16, bf) == 3
-    assert q(2, 100, 256, 1, 2, 32, bf) == 1          # R = 32: forward only
+    for R in (8, 24, 32):                              # ranks padded to 16 or 32 on chip
+        assert q(2, 100, 256, 1, 2, R, bf) == 3
     # everything else takes the CUDA-core kernels
     assert q(8, 2048, 6144, 1, 4, 16, f32) == 0        # fp32 keeps exact fp32 filters
     assert q(8, 2048, 6144, 4, 4, 16, bf) == 0         # tied filters (H > 1)
-    assert q(8, 2048, 6144, 1, 4, 8, bf) == 0
+    assert q(8, 2048, 6144, 1, 4, 12, bf) == 0         # R not a multiple of 8
     # invalid or unbuilt arguments
     assert q(8, 2048, 6144, 1, 4, 0, bf) == -1
     assert q(8, 2048, 6144, 1, 5, 16, bf) == -1

@@ -1,6 +1,7 @@
 """GPU parity of the tensor-core (tcgen05) low-rank kernels against the fp64
 oracle, on shapes chosen for that path: bf16, per-channel filters (H = 1),
-R = 16 or 32, every W, several 64-channel chunks and 128-token tiles with
+R in {8, 16, 24, 32} (ranks below a multiple of 16 padded with zeros on
+chip), every W, several 64-channel chunks and 128-token tiles with
 ragged tails, sequences shorter than the causal window, and channel counts
 that are not a multiple of the 64-channel chunk.  Each case first checks
 that the library does route it to the tensor cores, and every test checks
@@ -36,8 +37,8 @@ def run_fwd(wl, seed):
 
 
 @pytest.mark.parametrize("W", [1, 2, 3, 4])
-@pytest.mark.parametrize("R", [16, 32])
-def test_fwd_every_width_both_ranks(W, R):
+@pytest.mark.parametrize("R", [8, 16, 24, 32])
+def test_fwd_every_width_every_rank(W, R):
     wl = syn.Workload("tc_fwd", B=2, T=300, C=320, W=W, H=1, R=R, residual=True,
                       zu_std=R ** -0.5)
     y, ry = run_fwd(wl, seed=10 * W + R)
@@ -98,9 +99,18 @@ def run_bwd(wl, seed):
 
 
 @pytest.mark.parametrize("W", [1, 2, 3, 4])
-def test_bwd_every_width(W):
-    wl = syn.Workload("tc_bwd", B=2, T=300, C=320, W=W, H=1, R=16, residual=True)
-    run_bwd(wl, seed=20 + W)
+@pytest.mark.parametrize("R", [8, 16, 24, 32])
+def test_bwd_every_width_every_rank(W, R):
+    wl = syn.Workload("tc_bwd", B=2, T=300, C=320, W=W, H=1, R=R, residual=True,
+                      zu_std=R ** -0.5)
+    run_bwd(wl, seed=20 + W + R)
+
+
+@pytest.mark.parametrize("R", [8, 32])
+def test_bwd_other_ranks_many_chunks_and_tiles(R):
+    # R = 32 holds at most 4 token tiles per split in TMEM: many splits
+    wl = syn.Workload("tc_bwd_big_r", B=4, T=1024, C=2048, W=4, H=1, R=R, zu_std=R ** -0.5)
+    run_bwd(wl, seed=90 + R)
 
 
 @pytest.mark.parametrize("residual", [False, True])
