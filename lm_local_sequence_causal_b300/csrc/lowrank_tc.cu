@@ -74,15 +74,19 @@ constexpr uint32_t kTmemCols = 512;
 
 __host__ __device__ constexpr int round1k(int b) { return (b + 1023) / 1024 * 1024; }
 
-template <int W, int KS>
+// HP = min(H, 8): channels of an 8-channel piece that share one filter.  A
+// 64-channel chunk uses (64/H)*W consecutive columns of U; they are loaded
+// as NA atoms of 64 columns (the tail of the last atom is not read back).
+template <int W, int KS, int HP>
 struct FwdLayout {
   static constexpr int XROWS = BM + W - 1;
   static constexpr int XBOX = XROWS * 128;            // bytes of one x box
   static constexpr int XBYTES = round1k(XBOX);
   static constexpr int ZBYTES = BM * 32;              // one K-step of z (4 KB)
-  static constexpr int NCOL = CC * W;                 // MMA N (U columns of the chunk)
+  static constexpr int NA = (W + HP - 1) / HP;        // 64-column U atoms per chunk
+  static constexpr int NCOL = 64 * NA;                // MMA N
   static constexpr int UATOM = KS * 16 * 128;         // 64 U columns x R rows (2 or 4 KB)
-  static constexpr int UBYTES = W * UATOM;
+  static constexpr int UBYTES = NA * UATOM;
   static constexpr int STAGE = XBYTES + KS * ZBYTES + round1k(UBYTES);
   static constexpr int YBYTES = BM * 128;             // staged y tile of one group
   static constexpr int Z_IN = XBYTES;                 // offsets inside a stage
@@ -142,12 +146,13 @@ __host__ __device__ constexpr uint32_t idesc_major(uint32_t M, uint32_t N, uint3
   return idesc_bf16_f32(M, N) | (amaj << 15) | (bmaj << 16);
 }
 
-template <int W, int KS>
+template <int W, int KS, int HP>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
           const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_y,
-          int ntiles, int nbt, int nchunks, int residual) {
-  using L = FwdLayout<W, KS>;
+          int ntiles, int nbt, int nchunks, int residual, int H) {
+  using L = FwdLayout<W, KS, HP>;
+  const int ucols = CC / H * W;              // U columns of one chunk
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1k(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -211,9 +216,9 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         for (int ks = 0; ks < KS; ++ks)
           tma_load_3d(st + L::Z_IN + ks * L::ZBYTES, &tm_z, full, ks * 16, itm.t0, itm.b,
                       pol_keep);
-        for (int a = 0; a < W; ++a)
-          tma_load_3d(st + L::U_IN + a * L::UATOM, &tm_u, full, itm.chunk * L::NCOL + a * 64, 0,
-                      0, pol_keep);
+        for (int a = 0; a < L::NA; ++a)
+          tma_load_3d(st + L::U_IN + a * L::UATOM, &tm_u, full, itm.chunk * ucols + a * 64, 0, 0,
+                      pol_keep);
       }
       // Let every load this thread issued land before the CTA can exit.
       for (int j = std::max(0, it - NST); j < it; ++j)
@@ -275,12 +280,14 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t xt = sb + s * L::STAGE;
-      // Four 8-channel chunks per warp; tap k of channel c is column c*W + k.
+      // Four 8-channel pieces per warp; tap k of the chunk's filter group gl
+      // is column gl*W + k, and channel c of the chunk uses group c / H.
+      constexpr int NCP = 8 / HP * W;        // TMEM columns of one piece
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int cch = 4 * h + q;           // 16-byte chunk of the 128-byte row
-        uint32_t acc[8 * W];
-        tmem_ld_cols<8 * W>(tbase + cch * 8 * W, acc);
+        uint32_t acc[NCP];
+        tmem_ld_cols<NCP>(tbase + (cch * 8 / H) * W, acc);
         float xv[W][8];
 #pragma unroll
         for (int k = 0; k < W; ++k)
@@ -292,7 +299,8 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         for (int c = 0; c < 8; ++c) {
           float v = residual ? xv[0][c] : 0.f;
 #pragma unroll
-          for (int k = 0; k < W; ++k) v = fmaf(__uint_as_float(acc[c * W + k]), xv[k][c], v);
+          for (int k = 0; k < W; ++k)
+            v = fmaf(__uint_as_float(acc[(c / HP) * W + k]), xv[k][c], v);
           out[c] = v;
         }
         sts128(ybuf + sw128_offset(tl, cch), pack16<__nv_bfloat16>(out));
@@ -813,13 +821,16 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 
 // U rearranged into the shared-memory image of the backward's U tiles: for
 // chunk ch and tap k, a [RP r][64 c] tile with 128-byte rows and the TMA
-// 128-byte swizzle, element (r, c) = U[r, (64*ch + c)*W + k] (zero past C
-// and for the padding ranks r >= R).
+// 128-byte swizzle, element (r, c) = U[r, ((64*ch + c)/H)*W + k] (zero past
+// C and for the padding ranks r >= R).  With tied filters (H > 1) every
+// channel gets its group's column, so the kernel sees per-channel filters
+// that are equal within a group; dU of a group is then the sum of the
+// per-channel dU over its H channels (the tied reduction below).
 template <int W, int RK>
 __global__ void lr_u_image(const __nv_bfloat16* __restrict__ U, unsigned char* __restrict__ img,
-                           int C, int R, int nchunks) {
+                           int C, int H, int R, int nchunks) {
   constexpr int RP = 16 * RK;
-  const int64_t CW = static_cast<int64_t>(C) * W;
+  const int64_t GW = static_cast<int64_t>(C / H) * W;
   const int total = nchunks * W * RP * 8;              // 16-byte pieces
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int piece = i & 7, r = (i >> 3) % RP, tile = (i >> 3) / RP;
@@ -833,7 +844,8 @@ __global__ void lr_u_image(const __nv_bfloat16* __restrict__ U, unsigned char* _
         const int c = ch * CC + piece * 8 + 2 * e + hh;
         uint32_t bits = 0;
         if (c < C && r < R)
-          bits = __bfloat16_as_ushort(U[static_cast<int64_t>(r) * CW + static_cast<int64_t>(c) * W + k]);
+          bits = __bfloat16_as_ushort(
+              U[static_cast<int64_t>(r) * GW + static_cast<int64_t>(c / H) * W + k]);
         pair |= bits << (16 * hh);
       }
       w4[e] = pair;
@@ -890,17 +902,38 @@ __global__ void lr_reduce_tc(const float* __restrict__ dz_part, const float* __r
   }
 }
 
+// Tied filters: dU[r, g*W + k] = sum_p sum_{h<H} dU_part[p][r][(g*H + h)*W + k],
+// p outer and h inner (a fixed order), one output a thread.
+__global__ void lr_reduce_du_tied(const float* __restrict__ dU_part,
+                                  __nv_bfloat16* __restrict__ dU, int R, int RP, int H, int W,
+                                  int64_t GW, int P) {
+  const int64_t CW = GW * H;
+  const int64_t total = static_cast<int64_t>(R) * GW;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / GW, j = i - r * GW;
+    const int64_t g = j / W, k = j - g * W;
+    const float* src = dU_part + r * CW + g * H * W + k;
+    float a = 0.f;
+    for (int p = 0; p < P; ++p) {
+      const float* sp = src + static_cast<int64_t>(p) * RP * CW;
+      for (int h = 0; h < H; ++h) a += __ldcs(sp + h * W);
+    }
+    dU[i] = __float2bfloat16_rn(a);
+  }
+}
+
 // ------------------------------------------------------------------ host ----
 
 
-template <int W, int KS>
+template <int W, int KS, int HP>
 cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, const Shape& s,
                        cudaStream_t st) {
-  using L = FwdLayout<W, KS>;
+  using L = FwdLayout<W, KS, HP>;
   CUtensorMap tx, tz, tu, ty;
   if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, BM + W - 1, 128) ||
       !make_tmap_3d(&tz, z, true, s.R, s.T, s.B, 16, BM, 32) ||
-      !make_tmap_3d(&tu, U, true, s.C * s.W, s.R, 1, 64, 16 * KS, 128) ||
+      !make_tmap_3d(&tu, U, true, s.G() * s.W, s.R, 1, 64, 16 * KS, 128) ||
       !make_tmap_3d(&ty, y, true, s.C, s.T, s.B, CC, BM, 128))
     return cudaErrorInvalidValue;
   const int ntiles = static_cast<int>((s.T + BM - 1) / BM);
@@ -910,11 +943,12 @@ cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, con
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   const long long grid = std::min<long long>(sms, items);
-  auto kern = lr_fwd_tc<W, KS>;
+  auto kern = lr_fwd_tc<W, KS, HP>;
   cudaError_t e = set_smem<L>(kern, L::TOTAL);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kFwdThreads, L::TOTAL, st>>>(
-      tx, tz, tu, ty, ntiles, static_cast<int>(nbt), nchunks, s.residual);
+      tx, tz, tu, ty, ntiles, static_cast<int>(nbt), nchunks, s.residual,
+      static_cast<int>(s.H));
   return cudaGetLastError();
 }
 
@@ -1018,7 +1052,7 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
     const int pieces = p.nchunks * W * L::RP * 8;
     lr_u_image<W, RK><<<std::min(1184, (pieces + 255) / 256), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(U), base + p.img_off, static_cast<int>(s.C),
-        static_cast<int>(s.R), p.nchunks);
+        static_cast<int>(s.H), static_cast<int>(s.R), p.nchunks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1029,18 +1063,49 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
   kern<<<static_cast<unsigned>(p.S * p.P), kBwdThreads, L::TOTAL, st>>>(tx, tdy, tz, tdx, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t nz4 = s.B * s.T * L::RP / 4, nU4 = s.R * s.C * s.W / 4;
+  // Per-channel dU partials reduce straight to dU when H = 1; tied filters
+  // add their H channels in a second small kernel.
+  const int64_t nz4 = s.B * s.T * L::RP / 4, nU4 = s.H == 1 ? s.R * s.C * s.W / 4 : 0;
   const int blocks = static_cast<int>(std::min<int64_t>((nz4 + nU4 + 255) / 256, 148 * 8));
   lr_reduce_tc<<<blocks, 256, 0, st>>>(a.dz_part, a.dU_part, static_cast<__nv_bfloat16*>(dz),
                                        static_cast<__nv_bfloat16*>(dU), nz4, p.S, nU4, p.P,
                                        static_cast<int>(s.R), L::RP, s.C * s.W);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || s.H == 1) return e;
+  const int64_t GW = s.G() * s.W;
+  const int tb = static_cast<int>(std::min<int64_t>((s.R * GW + 255) / 256, 148 * 8));
+  lr_reduce_du_tied<<<tb, 256, 0, st>>>(a.dU_part, static_cast<__nv_bfloat16*>(dU),
+                                        static_cast<int>(s.R), L::RP, static_cast<int>(s.H),
+                                        W, GW, p.P);
   return cudaGetLastError();
+}
+
+template <int KS, int HP>
+cudaError_t fwd_hp(const void* x, const void* z, const void* U, void* y, const Shape& s,
+                   cudaStream_t st) {
+  switch (s.W) {
+    case 1: return launch_fwd<1, KS, HP>(x, z, U, y, s, st);
+    case 2: return launch_fwd<2, KS, HP>(x, z, U, y, s, st);
+    case 3: return launch_fwd<3, KS, HP>(x, z, U, y, s, st);
+    default: return launch_fwd<4, KS, HP>(x, z, U, y, s, st);
+  }
+}
+
+template <int KS>
+cudaError_t fwd_w(const void* x, const void* z, const void* U, void* y, const Shape& s, int hp,
+                  cudaStream_t st) {
+  switch (hp) {
+    case 1: return fwd_hp<KS, 1>(x, z, U, y, s, st);
+    case 2: return fwd_hp<KS, 2>(x, z, U, y, s, st);
+    case 4: return fwd_hp<KS, 4>(x, z, U, y, s, st);
+    default: return fwd_hp<KS, 8>(x, z, U, y, s, st);
+  }
 }
 
 }  // namespace
 
 bool lowrank_bwd_tc_supported(const Shape& s) {
-  return s.bf16 && s.H == 1 && s.R >= 8 && s.R <= 32 && s.R % 8 == 0 && s.W >= 1 && s.W <= 4 &&
+  return s.bf16 && s.H >= 1 && s.R >= 8 && s.R <= 32 && s.R % 8 == 0 && s.W >= 1 && s.W <= 4 &&
          s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.T < (int64_t(1) << 30) &&
          s.C < (int64_t(1) << 24);
 }
@@ -1074,8 +1139,13 @@ cudaError_t lowrank_bwd_tc(const void* x, const void* z, const void* U, const vo
   }
 }
 
+// Forward: tied filters need whole groups in a 64-channel chunk and a U
+// column offset per chunk ((64/H)*W columns) on a 16-byte boundary, which
+// TMA requires; the U rows ((C/H)*W columns) must be a multiple of 16 bytes.
 bool lowrank_tc_supported(const Shape& s) {
-  return s.bf16 && s.H == 1 && s.R >= 8 && s.R <= 32 && s.R % 8 == 0 && s.W >= 1 && s.W <= 4 &&
+  const bool tie_ok = s.H == 1 || (s.H <= 64 && 64 % s.H == 0 && (64 / s.H * s.W) % 8 == 0 &&
+                                   (s.G() * s.W) % 8 == 0);
+  return s.bf16 && tie_ok && s.R >= 8 && s.R <= 32 && s.R % 8 == 0 && s.W >= 1 && s.W <= 4 &&
          s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.T < (int64_t(1) << 30) &&
          s.C < (int64_t(1) << 24);
 }
@@ -1083,12 +1153,10 @@ bool lowrank_tc_supported(const Shape& s) {
 cudaError_t lowrank_fwd_tc(const void* x, const void* z, const void* U, void* y,
                            const Shape& s, cudaStream_t st) {
   if (!lowrank_tc_supported(s)) return cudaErrorNotSupported;
-  const bool k2 = s.R > 16;
-  switch (s.W) {
-    case 1: return k2 ? launch_fwd<1, 2>(x, z, U, y, s, st) : launch_fwd<1, 1>(x, z, U, y, s, st);
-    case 2: return k2 ? launch_fwd<2, 2>(x, z, U, y, s, st) : launch_fwd<2, 1>(x, z, U, y, s, st);
-    case 3: return k2 ? launch_fwd<3, 2>(x, z, U, y, s, st) : launch_fwd<3, 1>(x, z, U, y, s, st);
-    default: return k2 ? launch_fwd<4, 2>(x, z, U, y, s, st) : launch_fwd<4, 1>(x, z, U, y, s, st);
+  const int hp = s.H >= 8 ? 8 : static_cast<int>(s.H);
+  switch (s.R > 16 ? 2 : 1) {
+    case 1: return fwd_w<1>(x, z, U, y, s, hp, st);
+    default: return fwd_w<2>(x, z, U, y, s, hp, st);
   }
 }
 

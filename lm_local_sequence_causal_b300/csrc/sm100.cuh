@@ -240,19 +240,52 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
-// Load n (8, 16, 24 or 32) consecutive columns.
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
+// Load n consecutive columns (n = 1..4, 6, 8, 12, 16, 24 or 32).
 template <int n>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
-  static_assert(n == 8 || n == 16 || n == 24 || n == 32, "column count");
+  static_assert(n == 1 || n == 2 || n == 3 || n == 4 || n == 6 || n == 8 || n == 12 ||
+                    n == 16 || n == 24 || n == 32,
+                "column count");
   if constexpr (n == 32) {
     tmem_ld32(taddr, r);
-  } else if constexpr (n == 16) {
-    tmem_ld16(taddr, r);
   } else if constexpr (n == 24) {
     tmem_ld16(taddr, r);
     tmem_ld8(taddr + 16, *reinterpret_cast<uint32_t(*)[8]>(r + 16));
-  } else {
+  } else if constexpr (n == 16) {
+    tmem_ld16(taddr, r);
+  } else if constexpr (n == 12) {
     tmem_ld8(taddr, *reinterpret_cast<uint32_t(*)[8]>(r));
+    tmem_ld4(taddr + 8, r + 8);
+  } else if constexpr (n == 8) {
+    tmem_ld8(taddr, *reinterpret_cast<uint32_t(*)[8]>(r));
+  } else if constexpr (n == 6) {
+    tmem_ld4(taddr, r);
+    tmem_ld2(taddr + 4, r + 4);
+  } else if constexpr (n == 4) {
+    tmem_ld4(taddr, r);
+  } else if constexpr (n == 3) {
+    tmem_ld2(taddr, r);
+    tmem_ld1(taddr + 2, r + 2);
+  } else if constexpr (n == 2) {
+    tmem_ld2(taddr, r);
+  } else {
+    tmem_ld1(taddr, r);
   }
 }
 

@@ -132,7 +132,10 @@ def test_lowrank_path_query():
         assert q(2, 100, 256, 1, 2, R, bf) == 3
     # everything else takes the CUDA-core kernels
     assert q(8, 2048, 6144, 1, 4, 16, f32) == 0        # fp32 keeps exact fp32 filters
-    assert q(8, 2048, 6144, 4, 4, 16, bf) == 0         # tied filters (H > 1)
+    for H in (2, 4, 8, 16, 32):                        # tied filters
+        assert q(8, 2048, 6144, H, 4, 16, bf) == 3
+    assert q(2, 100, 6144, 32, 3, 16, bf) == 2         # (64/H)*W = 6: U offsets off 16 B
+    assert q(2, 100, 200, 8, 4, 16, bf) == 2           # rows of U (G*W = 100) off 16 B
     assert q(8, 2048, 6144, 1, 4, 12, bf) == 0         # R not a multiple of 8
     # invalid or unbuilt arguments
     assert q(8, 2048, 6144, 1, 4, 0, bf) == -1

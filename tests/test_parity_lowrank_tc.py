@@ -1,6 +1,6 @@
 """GPU parity of the tensor-core (tcgen05) low-rank kernels against the fp64
-oracle, on shapes chosen for that path: bf16, per-channel filters (H = 1),
-R in {8, 16, 24, 32} (ranks below a multiple of 16 padded with zeros on
+oracle, on shapes chosen for that path: bf16, per-channel filters (H = 1)
+and filters tied over H channels, R in {8, 16, 24, 32} (ranks below a multiple of 16 padded with zeros on
 chip), every W, several 64-channel chunks and 128-token tiles with
 ragged tails, sequences shorter than the causal window, and channel counts
 that are not a multiple of the 64-channel chunk.  Each case first checks
@@ -145,3 +145,49 @@ def test_bwd_repeated_calls_are_identical():
     b = dsc.lowrank_bwd(inp["x"], inp["z"], inp["U"], inp["dy"], 1, 4, True)
     for p, q in zip(a, b):
         assert torch.equal(p, q)
+
+
+# Tied filters (H > 1): the forward reads the chunk's (64/H)*W U columns and
+# each channel picks its group's taps; the backward sees per-channel filters
+# equal within a group and adds the group's H channels for dU.
+@pytest.mark.parametrize("H", [2, 4, 8, 16, 32])
+@pytest.mark.parametrize("W", [2, 3, 4])
+def test_tied_fwd_and_bwd(H, W):
+    wl = syn.Workload("tc_tied", B=2, T=300, C=320, W=W, H=H, R=16, residual=True)
+    q = dsc.dsc_lowrank_uses_tensor_cores(wl.B, wl.T, wl.C, H, W, 16, wl.dtype)
+    assert q & 2
+    if q & 1:
+        y, ry = run_fwd(wl, seed=40 + H + W)
+        assert_fwd(y, ry, wl.dtype)
+    run_bwd(wl, seed=50 + H + W)
+
+
+@pytest.mark.parametrize("R", [8, 32])
+def test_tied_other_ranks_and_a_ragged_chunk(R):
+    # C = 200: the last chunk holds 8 channels; G*W = 100 keeps the forward
+    # off the tensor cores, the backward stays on them
+    wl = syn.Workload("tc_tied_r", B=2, T=257, C=200, W=4, H=8, R=R, zu_std=R ** -0.5)
+    run_bwd(wl, seed=60 + R)
+    wl2 = syn.Workload("tc_tied_r2", B=2, T=257, C=448, W=4, H=8, R=R, zu_std=R ** -0.5)
+    y, ry = run_fwd(wl2, seed=61 + R)
+    assert_fwd(y, ry, wl2.dtype)
+    run_bwd(wl2, seed=62 + R)
+
+
+def test_tied_qkv_size_sampled():
+    # the QKV shape with head-wise tying H = 16 on the low-rank path
+    wl = syn.Workload("tc_tied_qkv", B=8, T=2048, C=6144, W=4, H=16, R=16)
+    assert dsc.dsc_lowrank_uses_tensor_cores(8, 2048, 6144, 16, 4, 16, wl.dtype) == 3
+    inp = syn.make_inputs(wl, 9, device="cuda")
+    y = dsc.lowrank_fwd(inp["x"], inp["z"], inp["U"], 16, 4, True)
+    dx, dz, dU = dsc.lowrank_bwd(inp["x"], inp["z"], inp["U"], inp["dy"], 16, 4, True)
+    torch.cuda.synchronize()
+    rows = syn.sample_rows(8, 2048, 4, 1024, seed=5)
+    from _parity import rows_of
+    ry = orc.lowrank_fwd(inp["x"], inp["z"], inp["U"], 16, 4, True, rows=rows)
+    assert_fwd(rows_of(y, rows), ry, wl.dtype)
+    rdx, rdz = orc.lowrank_bwd_rows(inp["x"], inp["z"], inp["U"], inp["dy"], 16, 4, True, rows=rows)
+    assert_grad(rows_of(dx, rows), rdx, wl.dtype, "dx")
+    assert_grad(rows_of(dz, rows), rdz, wl.dtype, "dz")
+    rdU = orc.lowrank_dU(inp["x"], inp["z"], inp["dy"], 16, 4)
+    assert_grad(dU, rdU, wl.dtype, "dU")
