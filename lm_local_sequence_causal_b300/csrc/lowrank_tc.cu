@@ -150,9 +150,9 @@ template <int W, int KS, int HP>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
           const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_y,
-          int ntiles, int nbt, int nchunks, int residual, int H) {
+          int ntiles, int nbt, int nchunks, int residual, int hshift) {
   using L = FwdLayout<W, KS, HP>;
-  const int ucols = CC / H * W;              // U columns of one chunk
+  const int ucols = (CC >> hshift) * W;      // U columns of one chunk (H = 2^hshift)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1k(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -287,7 +287,9 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       for (int q = 0; q < 4; ++q) {
         const int cch = 4 * h + q;           // 16-byte chunk of the 128-byte row
         uint32_t acc[NCP];
-        tmem_ld_cols<NCP>(tbase + (cch * 8 / H) * W, acc);
+        // first filter group of the piece: cch*8/H (H = HP below 8)
+        const int g0 = HP < 8 ? cch * 8 / HP : (cch * 8) >> hshift;
+        tmem_ld_cols<NCP>(tbase + g0 * W, acc);
         float xv[W][8];
 #pragma unroll
         for (int k = 0; k < W; ++k)
@@ -948,7 +950,7 @@ cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, con
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kFwdThreads, L::TOTAL, st>>>(
       tx, tz, tu, ty, ntiles, static_cast<int>(nbt), nchunks, s.residual,
-      static_cast<int>(s.H));
+      __builtin_ctzll(static_cast<unsigned long long>(s.H)));
   return cudaGetLastError();
 }
 
@@ -1143,7 +1145,8 @@ cudaError_t lowrank_bwd_tc(const void* x, const void* z, const void* U, const vo
 // column offset per chunk ((64/H)*W columns) on a 16-byte boundary, which
 // TMA requires; the U rows ((C/H)*W columns) must be a multiple of 16 bytes.
 bool lowrank_tc_supported(const Shape& s) {
-  const bool tie_ok = s.H == 1 || (s.H <= 64 && 64 % s.H == 0 && (64 / s.H * s.W) % 8 == 0 &&
+  const bool pow2 = (s.H & (s.H - 1)) == 0;
+  const bool tie_ok = s.H == 1 || (pow2 && s.H <= 64 && (64 / s.H * s.W) % 8 == 0 &&
                                    (s.G() * s.W) % 8 == 0);
   return s.bf16 && tie_ok && s.R >= 8 && s.R <= 32 && s.R % 8 == 0 && s.W >= 1 && s.W <= 4 &&
          s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.T < (int64_t(1) << 30) &&
