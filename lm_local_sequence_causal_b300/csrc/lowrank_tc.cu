@@ -391,9 +391,9 @@ struct BwdLayout {
   static constexpr int DW_OFF = U_OFF + 2 * UALLOC;
   static constexpr int DX_OFF = DW_OFF + NT * DWTAP;
   static constexpr int BAR_OFF = DX_OFF + BM * 128;
-  // full[3] empty[3] dfull dempty dwfull[2] dwfree[2] ufull[2] ufree[2]
+  // full[3] empty[3] dfull[2] dempty[2] dwfull[2] dwfree[2] ufull[2] ufree[2]
   // uafull[2] uaempty[2] dzfull yfull yfree
-  static constexpr int NBAR = 2 * NSTB + 2 + 4 + 8 + 3;
+  static constexpr int NBAR = 2 * NSTB + 4 + 4 + 8 + 3;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int TOTAL = MISC_OFF + 16 + 1024;
   static constexpr uint32_t TX = 2 * XBOX + ZBOX;
@@ -437,9 +437,9 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 
   const uint32_t bar_full = sb + L::BAR_OFF;
   const uint32_t bar_empty = bar_full + NST_ * 8;
-  const uint32_t bar_dfull = bar_empty + NST_ * 8;
-  const uint32_t bar_dempty = bar_dfull + 8;
-  const uint32_t bar_dwfull = bar_dempty + 8;    // [2]: one per tap pair of the dw tiles
+  const uint32_t bar_dfull = bar_empty + NST_ * 8;  // [2]: one per 32-channel half of D
+  const uint32_t bar_dempty = bar_dfull + 16;       // [2]
+  const uint32_t bar_dwfull = bar_dempty + 16;   // [2]: one per tap pair of the dw tiles
   const uint32_t bar_dwfree = bar_dwfull + 16;   // [2]
   const uint32_t bar_ufull = bar_dwfree + 16;
   const uint32_t bar_ufree = bar_ufull + 16;
@@ -456,8 +456,10 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 2 + 2 * NEPI);   // both MMA issuers, both groups
     }
-    mbar_init(bar_dfull, 1);
-    mbar_init(bar_dempty, NEPI);
+    for (int hh = 0; hh < 2; ++hh) {
+      mbar_init(bar_dfull + 8 * hh, 1);
+      mbar_init(bar_dempty + 8 * hh, NEPI);
+    }
     for (int pr = 0; pr < 2; ++pr) {
       mbar_init(bar_dwfull + 8 * pr, NEPI);
       mbar_init(bar_dwfree + 8 * pr, 1);
@@ -536,36 +538,49 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     }
   } else if (warp == 1) {
     // --------------------------------------------------- D-MMA issuer --
-    // D_k for every item, as soon as the dx group has freed D.
+    // D_k for every item in two 32-channel halves (N = 32), each as soon as
+    // the dx group has freed that half: the first half of item n+1 is
+    // formed while the dx group works on the second half of item n.
     if (lane == 0) {
-      constexpr uint32_t id_d = idesc_major(BM, 64, 0, 1);    // A z K-major, B U MN-major
+      constexpr uint32_t id_d = idesc_major(BM, 32, 0, 1);    // A z K-major, B U MN-major
       const uint32_t zsbo = L::XROWS * 16;                    // stride of the two z halves
-      int n = 0;
-      for (; n < nitems; ++n) {
+      int issued[2] = {0, 0};
+      bool ok = true;
+      for (int n = 0; n < nitems && ok; ++n) {
         const int lc = n / ntile, lt = n - lc * ntile;
         const int s = n % NST_;
-        bool ok = true;
         if (lt == 0)
           ok = mbar_wait(bar_ufull + 8 * (lc & 1), (lc >> 1) & 1, abort_flag, &g_tc_error, 2);
-        ok = ok && mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 2) &&
-             mbar_wait(bar_dempty, (n & 1) ^ 1, abort_flag, &g_tc_error, 2);
+        ok = ok && mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 2);
         if (!ok) break;
-        tc_fence_after();
         const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
         const uint32_t ut = sb + L::U_OFF + (lc & 1) * L::UALLOC;
 #pragma unroll
-        for (int k = 0; k < W; ++k)
+        for (int hh = 0; hh < 2; ++hh) {
+          ok = mbar_wait(bar_dempty + 8 * hh, (n & 1) ^ 1, abort_flag, &g_tc_error, 2);
+          if (!ok) break;
+          tc_fence_after();
+          // Half hh = channels 32*hh .. +31: columns k*64 + 32*hh of D, and
+          // U columns 32*hh .. of the chunk's tiles (64 bytes into each
+          // 128-byte swizzled row).
 #pragma unroll
-          for (int ks = 0; ks < RK; ++ks)
-            mma_bf16(tmem + L::TM_D + k * 64, make_desc(zt + 16 * k + 2 * ks * zsbo, zsbo, 128, 0),
-                     make_desc(ut + k * L::UTAP + ks * 2048, 16, 1024, 2), id_d,
-                     ks > 0 ? 1u : 0u);
-        mma_commit(bar_dfull);
+          for (int k = 0; k < W; ++k)
+#pragma unroll
+            for (int ks = 0; ks < RK; ++ks)
+              mma_bf16(tmem + L::TM_D + k * 64 + 32 * hh,
+                       make_desc(zt + 16 * k + 2 * ks * zsbo, zsbo, 128, 0),
+                       make_desc(ut + k * L::UTAP + ks * 2048 + 64 * hh, 16, 1024, 2), id_d,
+                       ks > 0 ? 1u : 0u);
+          mma_commit(bar_dfull + 8 * hh);
+          ++issued[hh];
+        }
+        if (!ok) break;
         mma_commit(bar_empty + 8 * s);
         if (lt == ntile - 1) mma_commit(bar_ufree + 8 * (lc & 1));
       }
       // Let every MMA this thread issued finish before TMEM is freed.
-      if (n > 0) drain_wait(bar_dfull, (n - 1) & 1);
+      for (int hh = 0; hh < 2; ++hh)
+        if (issued[hh] > 0) drain_wait(bar_dfull + 8 * hh, (issued[hh] - 1) & 1);
     }
   } else if (warp == kDzduWarp) {
     // ------------------------------------------------- dz/dU-MMA issuer --
@@ -657,19 +672,24 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int b = gt / args.ntiles, t0 = (gt - b * args.ntiles) * BM;
         const int c0 = (ch0 + lc) * CC;
         const uint32_t dyt = sb + L::STG_OFF + s * L::STAGE + L::XBYTES;
-        ok = mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3) &&
-             mbar_wait(bar_dfull, n & 1, abort_flag, &g_tc_error, 3);
+        ok = mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3);
         if (!__all_sync(0xffffffffu, ok)) break;
-        tc_fence_after();
         const bool row_ok = t0 + tl < args.T;
         __nv_bfloat16* dxrow = args.dx + (static_cast<int64_t>(b) * args.T + t0 + tl) * args.C + c0;
+        // The two 32-channel halves of D in turn; in each, the warp's lane
+        // group takes its tokens and the warp pair splits the 32 channels.
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_dfull + 8 * hh, n & 1, abort_flag, &g_tc_error, 3));
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int cch = 4 * h + q;
+        for (int q = 0; q < 2; ++q) {
+          const int cch = 4 * hh + 2 * h + q;
           uint32_t dk[W][8];
 #pragma unroll
           for (int k = 0; k < W; ++k)
-            tmem_ld8(tmem + tlane + L::TM_D + k * 64 + 32 * h + 8 * q, dk[k]);
+            tmem_ld8(tmem + tlane + L::TM_D + k * 64 + 8 * cch, dk[k]);
           uint4 gr[W];
           gr[0] = lds128(dyt + sw128_offset(tl, cch));
 #pragma unroll
@@ -699,10 +719,10 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar_dempty);
-          mbar_arrive(bar_empty + 8 * s);
+        if (lane == 0) mbar_arrive(bar_dempty + 8 * hh);
         }
+        if (!ok) break;
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
       }
     } else {
       // dw[t,c,k] = dy[t,c] x[t-k,c].  Thread (chunk wc of 8 channels, run of
