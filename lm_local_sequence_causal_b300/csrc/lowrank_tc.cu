@@ -70,6 +70,9 @@ constexpr int NEPI = 8;     // warps per backward epilogue group (4 lane groups 
 // producer, D-MMA issuer, dx group, dw group, dz/dU-MMA issuer
 constexpr int kBwdThreads = (3 + 2 * NEPI) * 32;
 constexpr int kDzduWarp = 2 + 2 * NEPI;
+// The backward's D accumulator is formed and handed to the dx warps in
+// kDParts channel parts of 64 / kDParts channels each.
+constexpr int kDParts = 2;
 constexpr uint32_t kTmemCols = 512;
 
 __host__ __device__ constexpr int round1k(int b) { return (b + 1023) / 1024 * 1024; }
@@ -391,9 +394,9 @@ struct BwdLayout {
   static constexpr int DW_OFF = U_OFF + 2 * UALLOC;
   static constexpr int DX_OFF = DW_OFF + NT * DWTAP;
   static constexpr int BAR_OFF = DX_OFF + BM * 128;
-  // full[3] empty[3] dfull[2] dempty[2] dwfull[2] dwfree[2] ufull[2] ufree[2]
-  // uafull[2] uaempty[2] dzfull yfull yfree
-  static constexpr int NBAR = 2 * NSTB + 4 + 4 + 8 + 3;
+  // full[3] empty[3] dfull[P] dempty[P] dwfull[2] dwfree[2] ufull[2] ufree[2]
+  // uafull[2] uaempty[2] dzfull yfull yfree  (P = kDParts)
+  static constexpr int NBAR = 2 * NSTB + 2 * kDParts + 4 + 8 + 3;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int TOTAL = MISC_OFF + 16 + 1024;
   static constexpr uint32_t TX = 2 * XBOX + ZBOX;
@@ -437,9 +440,9 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 
   const uint32_t bar_full = sb + L::BAR_OFF;
   const uint32_t bar_empty = bar_full + NST_ * 8;
-  const uint32_t bar_dfull = bar_empty + NST_ * 8;  // [2]: one per 32-channel half of D
-  const uint32_t bar_dempty = bar_dfull + 16;       // [2]
-  const uint32_t bar_dwfull = bar_dempty + 16;   // [2]: one per tap pair of the dw tiles
+  const uint32_t bar_dfull = bar_empty + NST_ * 8;     // [kDParts]: one per channel part of D
+  const uint32_t bar_dempty = bar_dfull + 8 * kDParts;  // [kDParts]
+  const uint32_t bar_dwfull = bar_dempty + 8 * kDParts;  // [2]: one per tap pair of the dw tiles
   const uint32_t bar_dwfree = bar_dwfull + 16;   // [2]
   const uint32_t bar_ufull = bar_dwfree + 16;
   const uint32_t bar_ufree = bar_ufull + 16;
@@ -456,7 +459,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 2 + 2 * NEPI);   // both MMA issuers, both groups
     }
-    for (int hh = 0; hh < 2; ++hh) {
+    for (int hh = 0; hh < kDParts; ++hh) {
       mbar_init(bar_dfull + 8 * hh, 1);
       mbar_init(bar_dempty + 8 * hh, NEPI);
     }
@@ -538,13 +541,14 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     }
   } else if (warp == 1) {
     // --------------------------------------------------- D-MMA issuer --
-    // D_k for every item in two 32-channel halves (N = 32), each as soon as
-    // the dx group has freed that half: the first half of item n+1 is
-    // formed while the dx group works on the second half of item n.
+    // D_k for every item in kDParts channel parts (N = 64 / kDParts), each
+    // as soon as the dx group has freed that part: the first part of item
+    // n+1 is formed while the dx group works on the last part of item n.
     if (lane == 0) {
-      constexpr uint32_t id_d = idesc_major(BM, 32, 0, 1);    // A z K-major, B U MN-major
+      constexpr int PW = CC / kDParts;                        // channels of a part
+      constexpr uint32_t id_d = idesc_major(BM, PW, 0, 1);    // A z K-major, B U MN-major
       const uint32_t zsbo = L::XROWS * 16;                    // stride of the two z halves
-      int issued[2] = {0, 0};
+      int issued[kDParts] = {};
       bool ok = true;
       for (int n = 0; n < nitems && ok; ++n) {
         const int lc = n / ntile, lt = n - lc * ntile;
@@ -556,20 +560,20 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
         const uint32_t ut = sb + L::U_OFF + (lc & 1) * L::UALLOC;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = 0; hh < kDParts; ++hh) {
           ok = mbar_wait(bar_dempty + 8 * hh, (n & 1) ^ 1, abort_flag, &g_tc_error, 2);
           if (!ok) break;
           tc_fence_after();
-          // Half hh = channels 32*hh .. +31: columns k*64 + 32*hh of D, and
-          // U columns 32*hh .. of the chunk's tiles (64 bytes into each
+          // Part hh = channels PW*hh .. +PW-1: columns k*64 + PW*hh of D, and
+          // U columns PW*hh .. of the chunk's tiles (2*PW*hh bytes into each
           // 128-byte swizzled row).
 #pragma unroll
           for (int k = 0; k < W; ++k)
 #pragma unroll
             for (int ks = 0; ks < RK; ++ks)
-              mma_bf16(tmem + L::TM_D + k * 64 + 32 * hh,
+              mma_bf16(tmem + L::TM_D + k * 64 + PW * hh,
                        make_desc(zt + 16 * k + 2 * ks * zsbo, zsbo, 128, 0),
-                       make_desc(ut + k * L::UTAP + ks * 2048 + 64 * hh, 16, 1024, 2), id_d,
+                       make_desc(ut + k * L::UTAP + ks * 2048 + 2 * PW * hh, 16, 1024, 2), id_d,
                        ks > 0 ? 1u : 0u);
           mma_commit(bar_dfull + 8 * hh);
           ++issued[hh];
@@ -579,7 +583,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         if (lt == ntile - 1) mma_commit(bar_ufree + 8 * (lc & 1));
       }
       // Let every MMA this thread issued finish before TMEM is freed.
-      for (int hh = 0; hh < 2; ++hh)
+      for (int hh = 0; hh < kDParts; ++hh)
         if (issued[hh] > 0) drain_wait(bar_dfull + 8 * hh, (issued[hh] - 1) & 1);
     }
   } else if (warp == kDzduWarp) {
@@ -676,16 +680,17 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         if (!__all_sync(0xffffffffu, ok)) break;
         const bool row_ok = t0 + tl < args.T;
         __nv_bfloat16* dxrow = args.dx + (static_cast<int64_t>(b) * args.T + t0 + tl) * args.C + c0;
-        // The two 32-channel halves of D in turn; in each, the warp's lane
-        // group takes its tokens and the warp pair splits the 32 channels.
+        // The channel parts of D in turn; in each, the warp's lane group
+        // takes its tokens and the warp pair splits the part's channels.
+        constexpr int PPC = CC / kDParts / 16;   // 8-channel pieces per warp and part
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = 0; hh < kDParts; ++hh) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar_dfull + 8 * hh, n & 1, abort_flag, &g_tc_error, 3));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int cch = 4 * hh + 2 * h + q;
+        for (int q = 0; q < PPC; ++q) {
+          const int cch = 2 * PPC * hh + PPC * h + q;
           uint32_t dk[W][8];
 #pragma unroll
           for (int k = 0; k < W; ++k)
