@@ -368,8 +368,8 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 // chunk), warp 1 TMEM owner and issuer of the D_k MMAs, warp 18 issuer of
 // the dz and dU MMAs (two issuers, so the dx path never waits behind the dw
 // path), warps 2-9 the dx group (reads
-// D_k and dy, writes dx through a staged TMA store and frees D so the MMAs
-// of the next item can start), warps 10-17 the dw group (forms dw into the
+// D_k and dy, writes dx from registers, and frees each 32-channel half of D
+// so the MMAs of the next item can start on it), warps 10-17 the dw group (forms dw into the
 // dw tiles one tap pair at a time; at chunk ends it reads out the dU
 // accumulator, at the end the dz ones).  The two groups run independently.
 
@@ -652,8 +652,8 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   } else {
     // ---------------------------------------------------------- epilogues --
     // Two groups of 8 warps that run independently, item by item:
-    //   warps 2-9   (dx group): dx = res*dy + sum_k D_k dy[t+k], staged and
-    //               stored with TMA; frees D for the next item's MMAs.
+    //   warps 2-9   (dx group): dx = res*dy + sum_k D_k dy[t+k], stored from
+    //               registers; frees each half of D for the next item's MMAs.
     //   warps 10-17 (dw group): dw tiles, one tap pair at a time; the dU
     //               readout at chunk ends and the dz readout at the end.
     // In each group warp (w % 4) owns TMEM lanes 32*(w % 4) .. +31 (tokens)
@@ -665,10 +665,11 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const uint32_t tlane = static_cast<uint32_t>(lg * 32) << 16;
     bool ok = true;
     if (dx_group) {
-      // dx[t] = res*dy[t] + sum_k D_k[t] dy[t+k]: each thread reads its own
-      // dy row; rows t+1..t+3 come from the neighbouring lanes, and only the
-      // last k lanes of a warp read row t+k from shared memory.  dx goes
-      // straight from registers to global memory.
+      // dx[t] = res*dy[t] + sum_k D_k[t] dy[t+k]: each thread reads dy rows
+      // t .. t+W-1 from the staged tile (the 128-byte swizzle keeps the 32
+      // rows of a warp's read conflict-free; measured as fast as passing
+      // rows between lanes by shuffles).  dx goes straight from registers to
+      // global memory.
       for (int n = 0; n < nitems; ++n) {
         const int lc = n / ntile, lt = n - lc * ntile;
         const int s = n % NST_;
@@ -698,13 +699,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
           uint4 gr[W];
           gr[0] = lds128(dyt + sw128_offset(tl, cch));
 #pragma unroll
-          for (int k = 1; k < W; ++k) {
-            gr[k].x = __shfl_down_sync(0xffffffffu, gr[0].x, k);
-            gr[k].y = __shfl_down_sync(0xffffffffu, gr[0].y, k);
-            gr[k].z = __shfl_down_sync(0xffffffffu, gr[0].z, k);
-            gr[k].w = __shfl_down_sync(0xffffffffu, gr[0].w, k);
-            if (lane >= 32 - k) gr[k] = lds128(dyt + sw128_offset(tl + k, cch));
-          }
+          for (int k = 1; k < W; ++k) gr[k] = lds128(dyt + sw128_offset(tl + k, cch));
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < W; ++k) tmem_regs_ready<8>(dk[k]);
