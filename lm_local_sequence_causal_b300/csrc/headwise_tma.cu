@@ -54,7 +54,6 @@ __host__ __device__ constexpr int round1k(int b) { return (b + 1023) / 1024 * 10
 template <int W, int H, bool BWD, int CW>
 struct HwLayout {
   static constexpr int NB = CW / 64;                  // 64-channel boxes per item
-  static constexpr int NST = BWD ? (NB == 1 ? 4 : 2) : (NB == 1 ? 4 : 3);
   static constexpr int GI = CW / H;                   // groups per item
   static constexpr int WROW = GI * W * 2;             // bytes of one token's taps
   static constexpr int WSW = (WROW == 32 || WROW == 64) ? WROW : 0;  // swizzle of the w box
@@ -70,6 +69,22 @@ struct HwLayout {
   static constexpr int OBOX = BM * 128;               // one staged 64-channel output box
   static constexpr int OBYTES = NB * OBOX;            // staged y / dx tile of one group
   static constexpr int DWBYTES = BWD ? round1k(BM * WROW) : 0;  // staged dw tile of one group
+  // Shared memory of the layout with `nst` stages.
+  static constexpr int total(int nst) {
+    return nst * STAGE + 2 * OBYTES + 2 * DWBYTES + (2 * nst + 4) * 8 + 16 + 1024;
+  }
+  // Stages: 6 in the forward when they fit (measured 87 instead of 94 us
+  // with 4 at the QKV size), else 4 when they fit, else 2.  Always even:
+  // the two epilogue groups take alternate items, so with an even count
+  // each stage serves one group only and a group waits on a stage's barrier
+  // at most one phase ahead of its last use.  With an odd count a stage
+  // alternates between the groups, a group can wait two phases ahead, and
+  // the parity wait then returns on the phase before (the data of the other
+  // group's item, still loading).
+  static constexpr int NST = (!BWD && total(6) <= 227 * 1024) ? 6
+                             : total(4) <= 227 * 1024            ? 4
+                                                                 : 2;
+  static_assert(NST % 2 == 0, "stages must be even");
   static constexpr int O_OFF = NST * STAGE;
   static constexpr int DW_OFF = O_OFF + 2 * OBYTES;
   static constexpr int BAR_OFF = DW_OFF + 2 * DWBYTES;
@@ -336,43 +351,79 @@ cudaError_t launch(const void* x, const void* dy, const void* w, void* out, void
 // bytes for the item's CW/H groups x W taps), with the narrowest item that
 // does: 64 channels for H = 8 (any W), (16, 2), (16, 4), (32, 4); 128
 // channels for (16, 1), (16, 3), (32, 2), (64, 4).
+// Channel width of the item for (H, W) and C, 0 if there is no TMA path.
+// The pairs are those whose filter rows make a TMA box of a multiple of 16
+// bytes.  The narrowest legal item is 64 channels for H = 8, (16, 2),
+// (16, 4) and (32, 4), 128 for (16, 1), (16, 3), (32, 2) and (64, 4).  The
+// forward of (8, 1), (16, 2) and (32, 4) takes 128-channel items when C
+// allows (measured 3 to 15% faster at C = 6144); for the others, (16, 4)
+// included, the wider item leaves room for only two stages and is slower.
+// The backward of (16, 3) has no TMA path: with 48-byte filter rows its two
+// stages, two staged outputs and two staged dw tiles do not fit shared
+// memory.
+int item_width(int64_t H, int64_t W, bool bwd, int64_t C) {
+  const bool narrow = (H == 8 && W >= 1 && W <= 4) || (H == 16 && (W == 2 || W == 4)) ||
+                      (H == 32 && W == 4);
+  const bool wide_only = (H == 16 && (W == 1 || W == 3)) || (H == 32 && W == 2) ||
+                         (H == 64 && W == 4);
+  const bool wide_fwd = (H == 8 && W == 1) || (H == 16 && W == 2) || (H == 32 && W == 4);
+  if (bwd && H == 16 && W == 3) return 0;
+  if (wide_only) return C % 128 == 0 ? 128 : 0;
+  if (!narrow) return 0;
+  if (!bwd && wide_fwd && C % 128 == 0) return 128;
+  return C % 64 == 0 ? 64 : 0;
+}
+
+template <bool BWD, int CW>
+cudaError_t dispatch_cw(const void* x, const void* dy, const void* w, void* out, void* dw,
+                        const Shape& s, cudaStream_t st) {
+  if constexpr (CW == 64) {
+    switch (s.H * 8 + s.W) {
+      case 8 * 8 + 1: return launch<1, 8, BWD, 64>(x, dy, w, out, dw, s, st);
+      case 8 * 8 + 2: return launch<2, 8, BWD, 64>(x, dy, w, out, dw, s, st);
+      case 8 * 8 + 3: return launch<3, 8, BWD, 64>(x, dy, w, out, dw, s, st);
+      case 8 * 8 + 4: return launch<4, 8, BWD, 64>(x, dy, w, out, dw, s, st);
+      case 16 * 8 + 2: return launch<2, 16, BWD, 64>(x, dy, w, out, dw, s, st);
+      case 16 * 8 + 4: return launch<4, 16, BWD, 64>(x, dy, w, out, dw, s, st);
+      case 32 * 8 + 4: return launch<4, 32, BWD, 64>(x, dy, w, out, dw, s, st);
+      default: break;
+    }
+  } else {
+    switch (s.H * 8 + s.W) {
+      case 16 * 8 + 1: return launch<1, 16, BWD, 128>(x, dy, w, out, dw, s, st);
+      case 16 * 8 + 3:
+        if constexpr (!BWD) return launch<3, 16, false, 128>(x, dy, w, out, dw, s, st);
+        break;
+      case 32 * 8 + 2: return launch<2, 32, BWD, 128>(x, dy, w, out, dw, s, st);
+      case 64 * 8 + 4: return launch<4, 64, BWD, 128>(x, dy, w, out, dw, s, st);
+      default: break;
+    }
+    if constexpr (!BWD) {
+      switch (s.H * 8 + s.W) {
+        case 8 * 8 + 1: return launch<1, 8, false, 128>(x, dy, w, out, dw, s, st);
+        case 16 * 8 + 2: return launch<2, 16, false, 128>(x, dy, w, out, dw, s, st);
+        case 32 * 8 + 4: return launch<4, 32, false, 128>(x, dy, w, out, dw, s, st);
+        default: break;
+      }
+    }
+  }
+  return cudaErrorNotSupported;
+}
+
 template <bool BWD>
 cudaError_t dispatch(const void* x, const void* dy, const void* w, void* out, void* dw,
                      const Shape& s, cudaStream_t st) {
-  switch (s.H * 8 + s.W) {
-    case 16 * 8 + 2: return launch<2, 16, BWD, 64>(x, dy, w, out, dw, s, st);
-    case 16 * 8 + 3:
-      if constexpr (!BWD) return launch<3, 16, BWD, 128>(x, dy, w, out, dw, s, st);
-      return cudaErrorNotSupported;
-    case 16 * 8 + 4: return launch<4, 16, BWD, 64>(x, dy, w, out, dw, s, st);
-    case 64 * 8 + 4: return launch<4, 64, BWD, 128>(x, dy, w, out, dw, s, st);
-    default: return cudaErrorNotSupported;
-  }
-}
-
-// Channel width of the item for (H, W), 0 if the pair has no TMA path.
-// The pairs routed here are the ones this kernel has run at full size
-// (many items per CTA): H = 16 with W = 2, 3 (forward only) and 4, and
-// H = 64 with W = 4.  The backward of (16, 3) does not fit shared memory
-// (48-byte filter rows: two stages, two staged outputs and two staged dw
-// tiles).  Other legal pairs (H = 8, H = 32, (16, 1)) take the
-// register-streaming kernels: the forward of (8, 1) at C = 6144, B = 8,
-// T = 2048 ended in a GPU fault that a build with every shared-memory
-// access and TMA coordinate checked did not reproduce, so the cause is not
-// known and those pairs stay off this kernel.
-int item_width(int64_t H, int64_t W, bool bwd) {
-  if (H == 16 && (W == 2 || W == 4)) return 64;
-  if (H == 16 && W == 3) return bwd ? 0 : 128;
-  if (H == 64 && W == 4) return 128;
-  return 0;
+  if (item_width(s.H, s.W, BWD, s.C) == 128)
+    return dispatch_cw<BWD, 128>(x, dy, w, out, dw, s, st);
+  return dispatch_cw<BWD, 64>(x, dy, w, out, dw, s, st);
 }
 
 }  // namespace
 
 bool headwise_tma_supported(const Shape& s, bool bwd) {
   if (!s.bf16) return false;
-  const int cw = item_width(s.H, s.W, bwd);
-  return cw > 0 && s.C % cw == 0 && s.T < (int64_t(1) << 30) &&
+  const int cw = item_width(s.H, s.W, bwd, s.C);
+  return cw > 0 && s.T < (int64_t(1) << 30) &&
          s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.C < (int64_t(1) << 24);
 }
 

@@ -137,21 +137,36 @@ using Raw = RawOf<kVB>::type;
 __device__ __forceinline__ Raw ldgv(const void* p) { return __ldg(reinterpret_cast<const Raw*>(p)); }
 __device__ __forceinline__ void stcsv(void* p, const Raw& v) { __stcs(reinterpret_cast<Raw*>(p), v); }
 
-__device__ __forceinline__ void raw_words(const uint32_t& u, uint32_t (&w)[1]) { w[0] = u; }
-__device__ __forceinline__ void raw_words(const uint2& u, uint32_t (&w)[2]) { w[0] = u.x; w[1] = u.y; }
-__device__ __forceinline__ void raw_words(const uint4& u, uint32_t (&w)[4]) {
-  w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+// The 32-bit words of a raw vector and back.
+template <typename R>
+__device__ __forceinline__ void raw_words(const R& u, uint32_t (&w)[sizeof(R) / 4]) {
+  if constexpr (sizeof(R) == 4) {
+    w[0] = u;
+  } else if constexpr (sizeof(R) == 8) {
+    w[0] = u.x;
+    w[1] = u.y;
+  } else {
+    w[0] = u.x;
+    w[1] = u.y;
+    w[2] = u.z;
+    w[3] = u.w;
+  }
 }
-__device__ __forceinline__ void words_raw(const uint32_t (&w)[1], uint32_t& u) { u = w[0]; }
-__device__ __forceinline__ void words_raw(const uint32_t (&w)[2], uint2& u) { u = make_uint2(w[0], w[1]); }
-__device__ __forceinline__ void words_raw(const uint32_t (&w)[4], uint4& u) {
-  u = make_uint4(w[0], w[1], w[2], w[3]);
+template <typename R>
+__device__ __forceinline__ void words_raw(const uint32_t (&w)[sizeof(R) / 4], R& u) {
+  if constexpr (sizeof(R) == 4) {
+    u = w[0];
+  } else if constexpr (sizeof(R) == 8) {
+    u = make_uint2(w[0], w[1]);
+  } else {
+    u = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 template <typename T>
 __device__ __forceinline__ void unpackv(const Raw& u, float (&f)[VecB<T>::N]) {
   uint32_t w[kVB / 4];
-  raw_words(u, w);
+  raw_words<Raw>(u, w);
 #pragma unroll
   for (int i = 0; i < kVB / 4; ++i) {
     if constexpr (sizeof(T) == 4) {
@@ -176,7 +191,7 @@ __device__ __forceinline__ Raw packv(const float (&f)[VecB<T>::N]) {
     }
   }
   Raw u;
-  words_raw(w, u);
+  words_raw<Raw>(w, u);
   return u;
 }
 

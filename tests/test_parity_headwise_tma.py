@@ -16,7 +16,8 @@ from _parity import Guarded, assert_fwd, assert_grad
 pytestmark = pytest.mark.gpu
 
 # (H, W, item width in channels)
-TMA_PAIRS = [(16, 2, 64), (16, 4, 64), (64, 4, 128)]
+TMA_PAIRS = [(8, 1, 64), (8, 2, 64), (8, 3, 64), (8, 4, 64), (16, 2, 64), (16, 4, 64),
+             (32, 4, 64), (16, 1, 128), (32, 2, 128), (64, 4, 128)]
 
 
 @pytest.fixture(autouse=True)
@@ -86,8 +87,19 @@ def test_routing():
     assert q(8, 2048, 6144, 16, 5, bf) == -1
 
 
-@pytest.mark.parametrize("H,W", [(8, 1), (8, 2), (8, 3), (8, 4), (16, 1), (32, 2), (32, 4)])
-def test_other_pairs_take_the_streaming_kernels(H, W):
-    # legal TMA boxes, but kept on the register-streaming kernels
-    wl = syn.Workload("hw_stream", B=2, T=300, C=640, W=W, H=H, residual=True)
-    check(wl, seed=H + W, paths=0)
+
+@pytest.mark.parametrize("H,W,CW", TMA_PAIRS)
+def test_many_items_per_cta(H, W, CW):
+    # 4 x 16 tiles x 16 chunks: every CTA takes about seven items, so each
+    # epilogue group reuses the pipeline stages (the forward with 128-channel
+    # items included)
+    wl = syn.Workload("hw_tma_multi", B=4, T=2048, C=16 * CW, W=W, H=H, residual=True)
+    check(wl, seed=H * 7 + W)
+
+
+@pytest.mark.parametrize("H,W", [(8, 1), (16, 2), (32, 4)])
+def test_wide_forward_items_of_narrow_pairs(H, W):
+    # C a multiple of 128: these forwards take 128-channel items (64-channel
+    # items when C is only a multiple of 64, as in the cases above)
+    wl = syn.Workload("hw_tma_wide", B=4, T=1024, C=2048, W=W, H=H, residual=True)
+    check(wl, seed=H * 5 + W)
