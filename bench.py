@@ -262,14 +262,14 @@ def sample_bytes(nseq, ntok):
 
 def cpu_baseline(prob):
     import oracle as orc
-    nseq, ntok = 2, 2048
+    nseq, ntok = 8, 2048          # the whole workload of the step
     s_hw = sample_inputs(prob.a, nseq, ntok)
     s_lr = sample_inputs(prob.b, nseq, ntok)
     sec = oracle_pass(s_hw, s_lr)
     gbs = sample_bytes(nseq, ntok) / sec / 1e9
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
             "sample": f"{nseq} of 8 sequences (T=2048, {nseq * ntok} tokens) of both "
-                      f"workloads, fwd+bwd, fp64, {sec:.2f} s",
+                      f"workloads, fwd+bwd, fp64, {sec:.2f} s on {orc.num_threads()} threads",
             "seconds": round(sec, 3), "mtok_per_s": round(nseq * ntok / sec / 1e6, 5)}
 
 
