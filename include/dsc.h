@@ -206,9 +206,10 @@ dsc_status_t dsc_lowrank_decode(const void* x, const void* z, const void* U, voi
 
 /*
  * Which low-rank kernels these arguments run on: bit 0 set if
- * dsc_lowrank_fwd uses the tensor cores (tcgen05: bf16, H = 1, R = 16 or
- * 32, 1 <= W <= 4), bit 1 set if dsc_lowrank_bwd does (bf16, H = 1,
- * R = 16, 1 <= W <= 4); a clear bit means the CUDA-core kernels.  -1 if the
+ * dsc_lowrank_fwd uses the tensor cores (tcgen05: bf16, R in {8, 16, 24,
+ * 32}, 1 <= W <= 4, H = 1, or H > 1 with (64/H)*W and (C/H)*W multiples of
+ * 8), bit 1 set if dsc_lowrank_bwd does (bf16, R in {8, 16, 24, 32},
+ * 1 <= W <= 4, any H); a clear bit means the CUDA-core kernels.  -1 if the
  * arguments are invalid or unsupported.  Host only; touches no device.
  */
 int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H,

@@ -57,13 +57,15 @@ cudaError_t lowrank_bwd(const void* x, const void* z, const void* U,
                         const void* dy, void* dx, void* dz, void* dU,
                         void* ws, const Shape& s, cudaStream_t st);
 
-// Tensor-core (tcgen05) low-rank kernels (lowrank_tc.cu): bf16, H = 1,
-// R in {16, 32}.  The *_tc functions return cudaErrorNotSupported when the
-// shape is outside that set, so the caller can use the CUDA-core kernels.
+// Tensor-core (tcgen05) low-rank kernels (lowrank_tc.cu): bf16, R in
+// {8, 16, 24, 32}, W <= 4, H = 1 or tied filters (the forward needs the
+// chunk's U columns on 16-byte boundaries, see lowrank_tc_supported).  The
+// *_tc functions return cudaErrorNotSupported when the shape is outside
+// that set, so the caller can use the CUDA-core kernels.
 bool lowrank_tc_supported(const Shape& s);
 cudaError_t lowrank_fwd_tc(const void* x, const void* z, const void* U, void* y,
                            const Shape& s, cudaStream_t st);
-// Backward on the tensor cores: bf16, H = 1, R = 16 (a subset of the above).
+// Backward on the tensor cores: bf16, R in {8, 16, 24, 32}, any H.
 bool lowrank_bwd_tc_supported(const Shape& s);
 size_t lowrank_bwd_tc_workspace(const Shape& s);
 cudaError_t lowrank_bwd_tc(const void* x, const void* z, const void* U, const void* dy,

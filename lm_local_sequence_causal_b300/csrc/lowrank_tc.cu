@@ -9,9 +9,10 @@
 //     Wt[128 tokens x 64*W columns] = Z[128 x R] * U[R x 64*W],
 // which the tensor core computes into TMEM (fp32, never rounded, never
 // written to memory); the CUDA cores then read each token's row of Wt and
-// apply the W taps to x.  The contraction has K = R = 16, so the tensor core
-// is busy for a few percent of the time; the kernel is built to stream x and
-// y at HBM speed around it.
+// apply the W taps to x.  The contraction has K = R (16 at the QKV size;
+// ranks up to 32, padded to 16 or 32 with zeros), so the tensor core is busy
+// for a few percent of the time; the kernel is built to stream x and y at
+// HBM speed around it.
 //
 // Forward kernel, one persistent CTA per SM, warp-specialised:
 //   warp 0      TMA producer: per work item (b, 128-token tile, 64-channel
