@@ -64,6 +64,10 @@ __device__ unsigned int g_tc_error = 0;
 constexpr int BM = 128;     // tokens per tile = TMEM lanes
 constexpr int CC = 64;      // channels per chunk = one 128-byte swizzled row
 constexpr int NST = 4;      // input pipeline stages
+// The forward's two epilogue groups take alternate items; an even stage
+// count keeps every stage with one group, so a group's parity wait on a
+// stage is never two phases ahead of the barrier.
+static_assert(NST % 2 == 0, "forward stages must be even");
 constexpr int NEPI_F = 16;  // forward epilogue warps: two groups of 8 that take alternate items
 constexpr int NGRP = 8;     // warps per forward epilogue group (4 lane groups x 2 channel halves)
 constexpr int kFwdThreads = (2 + NEPI_F) * 32;
