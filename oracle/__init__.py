@@ -6,8 +6,10 @@ the C ABI) never touches it, and it shares no code with them.
 
 The arithmetic lives in ``dsc_oracle.c`` (plain fp64 loops, one function per
 definition; see the comment block at its top for the passages each follows).
-This module only marshals torch CPU tensors into it and returns fp64 torch
-tensors.  Inputs may be float64, float32 or bfloat16; the C side decodes them
+This module marshals torch CPU tensors into it and returns fp64 torch
+tensors; the decode step and the static convolution at the end are
+compositions of those functions (a W-token window through the forward; the
+filter repeated at every token, its gradient summed over tokens in fp64).  Inputs may be float64, float32 or bfloat16; the C side decodes them
 exactly, so the oracle sees the values the GPU sees.
 
 Every function takes an optional ``rows`` (int64 tensor of token indices
