@@ -159,7 +159,8 @@ def sample_rows(B: int, T: int, W: int, n: int, seed: int = 0, tile: int = 64):
 
     It always holds the first W and last W tokens of every sequence and the
     tokens on either side of every `tile`-th position (where kernels switch
-    tiles), topped up with uniformly drawn rows to about n rows in total.
+    tiles), topped up with uniformly drawn distinct rows to at least
+    min(n, B*T) rows in total.
     """
     must = set()
     for b in range(B):
@@ -172,8 +173,15 @@ def sample_rows(B: int, T: int, W: int, n: int, seed: int = 0, tile: int = 64):
             for d in (-1, 0):
                 must.add(b * T + t0 + d)
     g = _gen(seed, 7, "cpu")
-    extra = max(0, n - len(must))
+    extra = min(max(0, n - len(must)), B * T - len(must))
     if extra:
-        draws = torch.randint(0, B * T, (extra,), generator=g).tolist()
-        must.update(draws)
+        # the first `extra` rows of a seeded permutation that are not yet in
+        # the set, so the result holds min(n, B*T) distinct rows (or more, if
+        # the edges and seams alone exceed n)
+        for r in torch.randperm(B * T, generator=g).tolist():
+            if r not in must:
+                must.add(r)
+                extra -= 1
+                if extra == 0:
+                    break
     return torch.tensor(sorted(must), dtype=torch.int64)

@@ -176,6 +176,24 @@ def lowrank_bwd_rows(x, z, U, dy, H, W, residual, rows=None, want_dw=False):
     return (dx, dz, dw) if want_dw else (dx, dz)
 
 
+def lowrank_dz(x, z, U, dy, H, W, rows=None):
+    """dz [B,T,R] (or [len(rows),R]) alone: the row-local low-rank backward
+    with the dx rows skipped (dz does not depend on them)."""
+    lib = _load()
+    B, T, C = x.shape
+    R = z.shape[-1]
+    xk, xp, xd = _in(x)
+    zk, zp, zd = _in(z)
+    uk, up, ud = _in(U)
+    gk, gp, gd = _in(dy)
+    rk, rp, n = _rows(rows, B * T)
+    dz = _out(n, R)
+    _check(lib.orc_lowrank_bwd_rows(
+        xp, xd, zp, zd, up, ud, gp, gd, None, ctypes.c_void_p(dz.data_ptr()), None,
+        B, T, C, H, W, R, 0, rp, n), "lowrank_dz")
+    return dz.view(B, T, R) if rows is None else dz
+
+
 def lowrank_dU(x, z, dy, H, W):
     """dU [R, G*W] = sum over all tokens of z_t^T dw_t, in token order."""
     lib = _load()
@@ -199,7 +217,7 @@ def lowrank_bwd(x, z, U, dy, H, W, residual):
 
 
 __all__ = ["headwise_fwd", "headwise_bwd", "lowrank_filters", "lowrank_fwd",
-           "lowrank_bwd_rows", "lowrank_dU", "lowrank_bwd", "num_threads",
+           "lowrank_bwd_rows", "lowrank_dz", "lowrank_dU", "lowrank_bwd", "num_threads",
            "set_num_threads", "LIB", "build_oracle"]
 
 

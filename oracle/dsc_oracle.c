@@ -266,8 +266,8 @@ int orc_lowrank_filters(const void* z, int zdt, const void* U, int Udt,
   return 0;
 }
 
-/* Row-local backward outputs: dx (always), dw (if dw != NULL), and for the
- * low-rank parameterisation dz (if dz != NULL). */
+/* Row-local backward outputs: dx (if dx != NULL), dw (if dw != NULL), and
+ * for the low-rank parameterisation dz (if dz != NULL). */
 static int run_bwd_rows(const void* x, int xdt, const void* dy, int dydt,
                         const filters_t* f, const shape_t* s,
                         const int64_t* rows, int64_t nrows, double* dx,
@@ -285,7 +285,7 @@ static int run_bwd_rows(const void* x, int xdt, const void* dy, int dydt,
 #pragma omp for schedule(static)
       for (int64_t i = 0; i < nrows; ++i) {
         const int64_t row = rows ? rows[i] : i;
-        dx_row(dy, dydt, f, s, row, wbuf, dx + i * s->C);
+        if (dx) dx_row(dy, dydt, f, s, row, wbuf, dx + i * s->C);
         if (dw || dz) {
           double* d = dw ? dw + i * GW : dwrow;
           dw_row(x, xdt, dy, dydt, s, row, d);
@@ -311,8 +311,9 @@ int orc_headwise_bwd(const void* x, int xdt, const void* w, int wdt,
                       dx, dw, NULL);
 }
 
-/* Low-rank backward, row-local part: dx [rows,C], dz [rows,R], and (if
- * dw != NULL) the intermediate dw [rows,G,W]. */
+/* Low-rank backward, row-local part: dx [rows,C] (if dx != NULL), dz
+ * [rows,R] (if dz != NULL), and (if dw != NULL) the intermediate dw
+ * [rows,G,W]. */
 int orc_lowrank_bwd_rows(const void* x, int xdt, const void* z, int zdt,
                          const void* U, int Udt, const void* dy, int dydt,
                          double* dx, double* dz, double* dw, int64_t B,

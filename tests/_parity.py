@@ -68,6 +68,24 @@ class Guarded:
         return bool((iv[:self.g] == s).all()) and bool((iv[self.g + self.n:] == s).all())
 
 
+def assert_by_channel_set(gpu, ref, hot, dtype, what, grad):
+    """The forward or gradient measure computed separately over the listed
+    `hot` channels and over all the others (last axis = channels), so that a
+    few large channels cannot hide errors in the ordinary ones."""
+    g = gpu.detach().double().cpu()
+    r = ref.double()
+    C = g.shape[-1]
+    mask = torch.zeros(C, dtype=torch.bool)
+    mask[hot] = True
+    out = {}
+    for name, m in (("hot", mask), ("ordinary", ~mask)):
+        e = (fro_rel if grad else max_rel)(g[..., m], r[..., m])
+        bound = TOL[dtype]["grad" if grad else "fwd"]
+        assert e <= bound, f"{what} ({name} channels): relative error {e:.3e} > {bound}"
+        out[name] = e
+    return out
+
+
 def rows_of(t, rows):
     """Rows (flattened tokens) of a [B,T,...] tensor, on the CPU."""
     flat = t.reshape(t.shape[0] * t.shape[1], -1)

@@ -264,6 +264,8 @@ def test_lowrank_gradients_match_finite_differences(H, W, R, res):
     assert torch.allclose(dx, _fd(L, x), rtol=1e-10, atol=1e-10)
     assert torch.allclose(dz, _fd(L, z), rtol=1e-10, atol=1e-10)
     assert torch.allclose(dU, _fd(L, U), rtol=1e-10, atol=1e-10)
+    # dz on its own (the row-local backward with dx skipped) is the same dz
+    assert torch.allclose(orc.lowrank_dz(x, z, U, dy, H, W), _fd(L, z), rtol=1e-10, atol=1e-10)
 
 
 # ---------------------------------------------- algebraic identities --------
@@ -336,6 +338,8 @@ def test_row_subsets_equal_full_outputs():
     dxs, dzs = orc.lowrank_bwd_rows(x, z, U, dy, H, W, True, rows=rows)
     assert torch.equal(dxs, dxl.view(-1, C)[rows])
     assert torch.equal(dzs, dzl.view(-1, R)[rows])
+    assert torch.equal(orc.lowrank_dz(x, z, U, dy, H, W), dzl)
+    assert torch.equal(orc.lowrank_dz(x, z, U, dy, H, W, rows=rows), dzl.view(-1, R)[rows])
     yl = orc.lowrank_fwd(x, z, U, H, W, True)
     assert torch.equal(orc.lowrank_fwd(x, z, U, H, W, True, rows=rows), yl.view(-1, C)[rows])
 

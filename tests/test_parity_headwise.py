@@ -12,7 +12,7 @@ import torch
 
 import oracle as orc
 from lm_local_sequence_causal_b300 import dsc, synthetic as syn
-from _parity import Guarded, assert_fwd, assert_grad, rows_of
+from _parity import Guarded, assert_by_channel_set, assert_fwd, assert_grad, rows_of
 
 pytestmark = pytest.mark.gpu
 
@@ -48,9 +48,14 @@ def check_sampled(wl, seed=0, nrows=4096):
     rows = syn.sample_rows(wl.B, wl.T, wl.W, nrows, seed)
     ry = orc.headwise_fwd(x, w, wl.H, wl.residual, rows=rows)
     rdx, rdw = orc.headwise_bwd(x, w, dy, wl.H, wl.residual, rows=rows)
+    assert len(rows) >= nrows
     assert_fwd(rows_of(y, rows), ry, wl.dtype)
     assert_grad(rows_of(dx, rows), rdx, wl.dtype, "dx")
     assert_grad(rows_of(dw, rows), rdw.reshape(len(rows), -1), wl.dtype, "dw")
+    if wl.hot_frac > 0:
+        hot = syn.hot_channels(wl.C, wl.hot_frac, seed)
+        assert_by_channel_set(rows_of(y, rows), ry, hot, wl.dtype, "y", grad=False)
+        assert_by_channel_set(rows_of(dx, rows), rdx, hot, wl.dtype, "dx", grad=True)
 
 
 @pytest.mark.parametrize("residual", [False, True])
@@ -69,7 +74,7 @@ def test_linear_rnn_long_sequence():
 @pytest.mark.parametrize("wl", [w for w in syn.all_linear_sweep() if not w.lowrank],
                          ids=lambda w: w.name)
 def test_all_linear_sweep(wl):
-    check_sampled(wl, nrows=2048)
+    check_sampled(wl, nrows=4096)
 
 
 # Every H path (vector-split groups, shuffle-reduced groups, generic), every

@@ -2,15 +2,16 @@
 
 The oracle forms each token's filters z_t U in fp64 and runs the plain
 definition; the kernels generate the filters on-chip.  dU is a reduction
-over every token, so it is always compared in full; y, dx and dz are
-compared in full on small shapes and on a seeded row sample at full size.
+over every token and dz one over every channel, so both are compared in
+full at every shape; y and dx are compared in full on small shapes and on a
+seeded sample of at least 4096 token rows at full size.
 """
 import pytest
 import torch
 
 import oracle as orc
 from lm_local_sequence_causal_b300 import dsc, synthetic as syn
-from _parity import Guarded, assert_fwd, assert_grad, rows_of
+from _parity import Guarded, assert_by_channel_set, assert_fwd, assert_grad, rows_of
 
 pytestmark = pytest.mark.gpu
 
@@ -42,19 +43,24 @@ def check_full(wl, seed=0):
     assert_grad(dU, rdU, wl.dtype, "dU")
 
 
-def check_sampled(wl, seed=0, nrows=4096, full_dU=True):
+def check_sampled(wl, seed=0, nrows=4096):
+    """y and dx on a seeded sample of >= nrows token rows (sequence edges
+    and tile seams included); dz on every row; dU in full."""
     inp = syn.make_inputs(wl, seed, device="cuda")
     x, z, U, dy = inp["x"], inp["z"], inp["U"], inp["dy"]
     y, dx, dz, dU = run_lowrank(x, z, U, dy, wl.H, wl.W, wl.residual)
     rows = syn.sample_rows(wl.B, wl.T, wl.W, nrows, seed)
+    assert len(rows) >= nrows
     ry = orc.lowrank_fwd(x, z, U, wl.H, wl.W, wl.residual, rows=rows)
-    rdx, rdz = orc.lowrank_bwd_rows(x, z, U, dy, wl.H, wl.W, wl.residual, rows=rows)
+    rdx, _ = orc.lowrank_bwd_rows(x, z, U, dy, wl.H, wl.W, wl.residual, rows=rows)
     assert_fwd(rows_of(y, rows), ry, wl.dtype)
     assert_grad(rows_of(dx, rows), rdx, wl.dtype, "dx")
-    assert_grad(rows_of(dz, rows), rdz, wl.dtype, "dz")
-    if full_dU:
-        rdU = orc.lowrank_dU(x, z, dy, wl.H, wl.W)
-        assert_grad(dU, rdU, wl.dtype, "dU")
+    assert_grad(dz, orc.lowrank_dz(x, z, U, dy, wl.H, wl.W), wl.dtype, "dz")
+    assert_grad(dU, orc.lowrank_dU(x, z, dy, wl.H, wl.W), wl.dtype, "dU")
+    if wl.hot_frac > 0:
+        hot = syn.hot_channels(wl.C, wl.hot_frac, seed)
+        assert_by_channel_set(rows_of(y, rows), ry, hot, wl.dtype, "y", grad=False)
+        assert_by_channel_set(rows_of(dx, rows), rdx, hot, wl.dtype, "dx", grad=True)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -76,7 +82,7 @@ def test_linear_rnn_long_sequence():
 @pytest.mark.parametrize("wl", [w for w in syn.all_linear_sweep() if w.lowrank],
                          ids=lambda w: w.name)
 def test_all_linear_sweep(wl):
-    check_sampled(wl, nrows=1024, full_dU=(wl.C == 2048))
+    check_sampled(wl)
 
 
 @pytest.mark.parametrize("W", [1, 2, 3, 4])
