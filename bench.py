@@ -20,6 +20,10 @@ value is the bytes of all ranks over that time.
 short convolution (w [C, W]) next to head-wise DSC at H=1 and H=16, same
 shape, same GPU.
 
+--sweep adds a line with per-shape throughput (GB/s, fraction of the
+measured HBM peak, Mtokens/s) of the 27 all-linear placement shapes x both
+parameterisations and the linear-RNN shape, forward and backward.
+
 --impl reference times the fp64 CPU oracle on the host cores instead, each
 step a bounded sample (the first 128 tokens of one sequence) of the same
 workload; it prints the same JSON line with "impl": "reference".
@@ -56,6 +60,8 @@ KERNEL_BOUND = {"headwise_fwd": "hbm", "headwise_bwd": "hbm",
 # fp32 FMA peak of the CUDA cores: 148 SMs x 128 lanes x 2 flop x 2.032 GHz.
 ALU_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 FALLBACK_HBM_GBS = 6400.0
+# GPU spin before the timed region's start event (about 2 ms at 2 GHz).
+SPIN_CYCLES = 4_000_000
 
 
 # ------------------------------------------------------------ byte model ----
@@ -108,34 +114,60 @@ def recorded_traffic(name):
 # ------------------------------------------------------------ clocks --------
 
 class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms from before
+    the warm-up until after the timed region (the region itself can be as
+    short as ten milliseconds); only samples taken between mark() and stop()
+    are summarised."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device):
+        import threading
         self.proc = None
+        self.lines = []            # (host time, line)
+        self.t_mark = None
         try:
             uuid = str(torch.cuda.get_device_properties(device).uuid)
             gid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", gid],
+                 "-lms", "20", "-i", gid],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        t0 = time.time()                       # wait for the first sample (at most 5 s)
+        while not self.lines and time.time() - t0 < 5 and self.proc.poll() is None:
+            time.sleep(0.01)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line))
+
+    def mark(self):
+        """Start of the window that stop() summarises (before the warm-up)."""
+        self.t_mark = time.perf_counter()
 
     def stop(self):
         if self.proc is None:
             return None
+        n_end = len(self.lines)
+        t0 = time.time()                       # one more sample after the timed region
+        while len(self.lines) <= n_end and time.time() - t0 < 1 and self.proc.poll() is None:
+            time.sleep(0.005)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
         sm, mx, reasons = [], [], set()
-        for line in out.strip().splitlines():
+        for t, line in self.lines:
+            if self.t_mark is not None and t < self.t_mark:
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -150,7 +182,8 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "warm-up and timed region, 20 ms interval"}
 
 
 # ------------------------------------------------------------ the step ------
@@ -174,6 +207,8 @@ class Problem:
         self.ws = dsc.lowrank_workspace(b["x"], b["z"], self.lr.H, self.lr.W)
 
     def calls(self):
+        """The four C calls of one step through the public binding (what a
+        user writes); every call re-marshals its arguments."""
         a, b, hw, lr = self.a, self.b, self.hw, self.lr
         return [
             ("headwise_fwd", lambda: dsc.dsc_headwise_fwd(a["x"], a["w"], self.y_hw, hw.H, True)),
@@ -184,6 +219,23 @@ class Problem:
             ("lowrank_bwd", lambda: dsc.dsc_lowrank_bwd(b["x"], b["z"], b["U"], b["dy"],
                                                         self.dx_lr, self.dz_lr, self.dU_lr,
                                                         self.ws, lr.H, lr.W, True)),
+        ]
+
+    def bound_calls(self, stream):
+        """The same four C calls with their arguments marshalled once
+        (dsc.bind), so that a timed loop spends its host time on the calls
+        themselves and the GPU is never left waiting on Python."""
+        a, b, hw, lr = self.a, self.b, self.hw, self.lr
+        return [
+            ("headwise_fwd", dsc.bind("dsc_headwise_fwd", a["x"], a["w"], self.y_hw, hw.H, True,
+                                      stream)),
+            ("headwise_bwd", dsc.bind("dsc_headwise_bwd", a["x"], a["w"], a["dy"], self.dx_hw,
+                                      self.dw_hw, hw.H, True, stream)),
+            ("lowrank_fwd", dsc.bind("dsc_lowrank_fwd", b["x"], b["z"], b["U"], self.y_lr,
+                                     lr.H, lr.W, True, stream)),
+            ("lowrank_bwd", dsc.bind("dsc_lowrank_bwd", b["x"], b["z"], b["U"], b["dy"],
+                                     self.dx_lr, self.dz_lr, self.dU_lr, self.ws, lr.H, lr.W,
+                                     True, stream)),
         ]
 
     # hw fwd, hw bwd, lr fwd, lr bwd (U image, main kernel, partial-sum reduction)
@@ -235,11 +287,22 @@ def max_over_ranks(v, ws):
 
 def oracle_pass(sample_hw, sample_lr):
     """One fp64 oracle pass of the hot path over a sample; returns seconds."""
+    return oracle_headwise(sample_hw) + oracle_lowrank(sample_lr)
+
+
+def oracle_headwise(hw):
+    """fp64 oracle forward + backward of the head-wise workload; seconds."""
     import oracle as orc
-    hw, lr = sample_hw, sample_lr
     t0 = time.perf_counter()
     orc.headwise_fwd(hw["x"], hw["w"], 16, True)
     orc.headwise_bwd(hw["x"], hw["w"], hw["dy"], 16, True)
+    return time.perf_counter() - t0
+
+
+def oracle_lowrank(lr):
+    """fp64 oracle forward + backward of the low-rank workload; seconds."""
+    import oracle as orc
+    t0 = time.perf_counter()
     orc.lowrank_fwd(lr["x"], lr["z"], lr["U"], 1, 4, True)
     orc.lowrank_bwd(lr["x"], lr["z"], lr["U"], lr["dy"], 1, 4, True)
     return time.perf_counter() - t0
@@ -260,17 +323,42 @@ def sample_bytes(nseq, ntok):
     return hf + hb + lf + lb
 
 
+def _leg(sec, nbytes, ntok):
+    return {"seconds": round(sec, 3), "gbs": round(nbytes / sec / 1e9, 4),
+            "mtok_per_s": round(ntok / sec / 1e6, 6)}
+
+
 def cpu_baseline(prob):
+    """The fp64 oracle on the host cores: the whole step (all 8 sequences of
+    both workloads) on every thread, and one sequence of each workload on
+    one thread; head-wise and low-rank legs timed separately."""
     import oracle as orc
-    nseq, ntok = 8, 2048          # the whole workload of the step
-    s_hw = sample_inputs(prob.a, nseq, ntok)
-    s_lr = sample_inputs(prob.b, nseq, ntok)
-    sec = oracle_pass(s_hw, s_lr)
-    gbs = sample_bytes(nseq, ntok) / sec / 1e9
-    return {"value": round(gbs, 3), "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
-            "sample": f"{nseq} of 8 sequences (T=2048, {nseq * ntok} tokens) of both "
-                      f"workloads, fwd+bwd, fp64, {sec:.2f} s on {orc.num_threads()} threads",
-            "seconds": round(sec, 3), "mtok_per_s": round(nseq * ntok / sec / 1e6, 5)}
+    allc = orc.num_threads()
+    hwb = sum(algorithmic(syn.qkv_headwise().with_(B=1))[:2])     # bytes per sequence
+    lrb = sum(algorithmic(syn.qkv_lowrank().with_(B=1))[:2])
+    T = 2048
+    legs = {}
+    s_hw, s_lr = sample_inputs(prob.a, 8, T), sample_inputs(prob.b, 8, T)
+    th, tl = oracle_headwise(s_hw), oracle_lowrank(s_lr)
+    legs["all_threads"] = {"threads": allc, "sample": "8 sequences (16384 tokens) per workload",
+                           "headwise_C1": _leg(th, 8 * hwb, 8 * T),
+                           "lowrank_C2": _leg(tl, 8 * lrb, 8 * T),
+                           "step": _leg(th + tl, 8 * (hwb + lrb), 8 * T)}
+    s_hw, s_lr = sample_inputs(prob.a, 1, T), sample_inputs(prob.b, 1, T)
+    orc.set_num_threads(1)
+    try:
+        th1, tl1 = oracle_headwise(s_hw), oracle_lowrank(s_lr)
+    finally:
+        orc.set_num_threads(allc)
+    legs["one_thread"] = {"threads": 1, "sample": "1 sequence (2048 tokens) per workload",
+                          "headwise_C1": _leg(th1, hwb, T), "lowrank_C2": _leg(tl1, lrb, T),
+                          "step": _leg(th1 + tl1, hwb + lrb, T)}
+    step = legs["all_threads"]["step"]
+    return {"value": step["gbs"], "unit": "GB/s", "cores": allc, "kind": "oracle",
+            "sample": f"whole step (8 of 8 sequences, 16384 tokens, of both workloads, fwd+bwd, "
+                      f"fp64) on {allc} threads: {step['seconds']} s; also one sequence of each "
+                      f"workload on 1 thread",
+            "seconds": step["seconds"], "mtok_per_s": step["mtok_per_s"], "legs": legs}
 
 
 def run_reference(args):
@@ -324,33 +412,40 @@ def run_dsc(args):
     dev = torch.device("cuda", local)
     dsc.load()
     prob = Problem(dev, seed=0)
-    calls = prob.calls()
+    stream = torch.cuda.current_stream()
+    calls = prob.bound_calls(stream)
     nbytes, nflops = prob.bytes_flops()
     step_bytes = sum(nbytes.values())
-    stream = torch.cuda.current_stream()
 
+    # The clock sampler runs from before the warm-up to after the timed
+    # region, and the timed region follows the warm-up with no idle gap.
+    clocks = ClockSampler(dev)
+    clocks.mark()
     for _ in range(args.warmup):
         for _, f in calls:
             f()
-    torch.cuda.synchronize()
-
-    # per-call events inside the timed region, on the launching stream
-    ev = {name: [] for name, _ in calls}
+    # per-call events inside the timed region, on the launching stream;
+    # created here so that the timed loop only records them
+    ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)] for name, _ in calls}
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev)
-    time.sleep(0.3)
-    barrier(ws)
     torch.cuda.synchronize()
+    barrier(ws)
+    # A short GPU spin ahead of the start event lets the host enqueue the
+    # first steps before the GPU reaches them, so the device-timed region
+    # holds kernels back to back rather than the host's launch latency (the
+    # host cost is reported separately, and the e2e line includes it).
+    torch.cuda._sleep(SPIN_CYCLES)
+    t_host = time.perf_counter()
     start.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
         for name, f in calls:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
+            e0, e1 = ev[name][i]
             e0.record(stream)
             f()
             e1.record(stream)
-            ev[name].append((e0, e1))
     end.record(stream)
+    host_ms = (time.perf_counter() - t_host) * 1e3 / args.steps
     torch.cuda.synchronize()
     barrier(ws)
     clk = clocks.stop()
@@ -359,7 +454,7 @@ def run_dsc(args):
     per_call_ms = {n: sum(a.elapsed_time(b) for a, b in v) / len(v) for n, v in ev.items()}
 
     # end to end: pinned host inputs -> device, the four calls, outputs -> host
-    e2e = run_e2e(prob, calls, args.e2e_steps) if args.e2e_steps > 0 else None
+    e2e = run_e2e(prob, prob.calls(), args.e2e_steps) if args.e2e_steps > 0 else None
     if e2e is not None:
         e2e_ms = max_over_ranks(e2e["ms_per_step"], ws)
         e2e["value"] = round(ws * step_bytes / (e2e_ms * 1e-3) / 1e9, 2)
@@ -403,6 +498,7 @@ def run_dsc(args):
                                   * 1e-3) / 1e6, 2)},
         "kernels": kernels, "roofline": roof,
         "gpu_launches": Problem.LAUNCHES_PER_STEP * args.steps,
+        "host_enqueue_ms_per_step": round(host_ms, 4),
         "clocks": clk,
     }
     if e2e is not None:
@@ -412,6 +508,8 @@ def run_dsc(args):
     print(json.dumps(line), flush=True)
     if args.compare_static:
         print(json.dumps(run_compare_static(dev, min(args.steps, 100))), flush=True)
+    if args.sweep:
+        print(json.dumps(run_sweep(dev, args.sweep_calls)), flush=True)
     return 0
 
 
@@ -458,6 +556,83 @@ def run_compare_static(dev, steps):
             "us": out}
 
 
+def _time_calls(f, n, stream, flush):
+    """Mean device time (ms) of n calls of f, each bracketed by its own event
+    pair, with `flush` (a write larger than L2) between calls and outside the
+    pairs; 3 warm-up calls first, and a GPU spin ahead of the first call keeps
+    the host ahead of the GPU."""
+    for _ in range(3):
+        f()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    torch.cuda._sleep(SPIN_CYCLES)
+    for a, b in ev:
+        flush()
+        a.record(stream)
+        f()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / n
+
+
+def run_sweep(dev, n):
+    """Throughput of every all-linear placement shape (C in {2048, 6144,
+    5632} x T in {512, 2048, 8192} at 16384 tokens x W in {2, 3, 4}, head-wise
+    H=16 and low-rank R=16) and of the linear-RNN shape (B=2, T=16384,
+    C=4096, W=4; H=64 and R=16), forward and backward timed separately."""
+    peak, peak_kind = measured_peaks()
+    stream = torch.cuda.current_stream()
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # 2x the L2
+
+    def flush():
+        scrub.fill_(1)
+
+    rows = []
+    wls = syn.all_linear_sweep() + [syn.linear_rnn_headwise(), syn.linear_rnn_lowrank()]
+    for wl in wls:
+        inp = syn.make_inputs(wl, 0, device=dev)
+        x, dy = inp["x"], inp["dy"]
+        y, dx = torch.empty_like(x), torch.empty_like(x)
+        if wl.lowrank:
+            z, U = inp["z"], inp["U"]
+            dz, dU = torch.empty_like(z), torch.empty_like(U)
+            ws = dsc.lowrank_workspace(x, z, wl.H, wl.W)
+            fwd = dsc.bind("dsc_lowrank_fwd", x, z, U, y, wl.H, wl.W, wl.residual, stream)
+            bwd = dsc.bind("dsc_lowrank_bwd", x, z, U, dy, dx, dz, dU, ws, wl.H, wl.W,
+                           wl.residual, stream)
+            path = dsc.dsc_lowrank_uses_tensor_cores(wl.B, wl.T, wl.C, wl.H, wl.W, wl.R,
+                                                     wl.dtype)
+            path = {"fwd": "tcgen05" if path & 1 else "cuda_cores",
+                    "bwd": "tcgen05" if path & 2 else "cuda_cores"}
+        else:
+            w = inp["w"]
+            dw = torch.empty_like(w)
+            fwd = dsc.bind("dsc_headwise_fwd", x, w, y, wl.H, wl.residual, stream)
+            bwd = dsc.bind("dsc_headwise_bwd", x, w, dy, dx, dw, wl.H, wl.residual, stream)
+            path = dsc.dsc_headwise_uses_tma(wl.B, wl.T, wl.C, wl.H, wl.W, wl.dtype)
+            path = {"fwd": "tma" if path & 1 else "register_streaming",
+                    "bwd": "tma" if path & 2 else "register_streaming"}
+        fb, bb, _, _ = algorithmic(wl)
+        tf, tb = _time_calls(fwd, n, stream, flush), _time_calls(bwd, n, stream, flush)
+        rows.append({
+            "name": wl.name, "B": wl.B, "T": wl.T, "C": wl.C, "W": wl.W, "H": wl.H,
+            "R": wl.R, "path": path,
+            "fwd_us": round(tf * 1e3, 1), "bwd_us": round(tb * 1e3, 1),
+            "fwd_gbs": round(fb / tf / 1e6, 1), "bwd_gbs": round(bb / tb / 1e6, 1),
+            "fwd_frac": round(fb / tf / 1e6 / peak, 4), "bwd_frac": round(bb / tb / 1e6 / peak, 4),
+            "fwd_bwd_gbs": round((fb + bb) / (tf + tb) / 1e6, 1),
+            "fwd_bwd_frac": round((fb + bb) / (tf + tb) / 1e6 / peak, 4),
+            "mtok_per_s": round(wl.tokens / ((tf + tb) * 1e-3) / 1e6, 2)})
+        del inp, x, dy, y, dx, fwd, bwd
+        torch.cuda.empty_cache()
+    return {"sweep": "all_linear_and_linear_rnn", "unit": "GB/s of algorithmic bytes",
+            "peak_gbs": peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+            "calls_per_point": n, "dtype": "bf16", "residual": True, "data": "synthetic",
+            "l2": "L2 flushed (256 MB write) before every timed call; each call timed by "
+                  "its own event pair", "rows": rows}
+
+
 def run_e2e(prob, calls, steps):
     """The same metric through the public API with host buffers: every step
     copies its inputs from pinned host memory and reads every output back."""
@@ -502,6 +677,12 @@ def main():
                     help="also print a second line: static short conv vs DSC latency")
     ap.add_argument("--compare-static-only", action="store_true",
                     help="print only the static-vs-DSC latency line (single GPU)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also print a line with per-shape throughput of the all-linear "
+                         "placement sweep and the linear-RNN shape")
+    ap.add_argument("--sweep-only", action="store_true",
+                    help="print only the sweep line (single GPU)")
+    ap.add_argument("--sweep-calls", type=int, default=20)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -512,6 +693,11 @@ def main():
         dsc.load()
         print(json.dumps(run_compare_static(torch.device("cuda", 0), min(args.steps, 100))),
               flush=True)
+        return 0
+    if args.sweep_only:
+        torch.cuda.set_device(0)
+        dsc.load()
+        print(json.dumps(run_sweep(torch.device("cuda", 0), args.sweep_calls)), flush=True)
         return 0
     return run_dsc(args)
 

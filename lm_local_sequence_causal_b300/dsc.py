@@ -9,6 +9,12 @@ If the library is missing the first call raises.
 
 ``headwise_fwd`` and friends are conveniences that allocate the outputs
 with torch and call the entry points.
+
+``bind(entry, *args, **kw)`` marshals the arguments of one entry point once
+and returns a ``BoundCall``: calling it re-issues the same C call with the
+same pointers, sizes and stream, with no per-call Python checks.  It is for
+loops that launch the same call on the same buffers many times, where the
+marshalling would otherwise cost more host time than the kernel takes.
 """
 import ctypes
 import os
@@ -66,6 +72,16 @@ def load():
     lib.dsc_lowrank_uses_tensor_cores.restype = INT
     lib.dsc_headwise_uses_tma.argtypes = [I64, I64, I64, I64, I64, INT]
     lib.dsc_headwise_uses_tma.restype = INT
+    lib.dsc_lowrank_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I64,
+                                            I64, INT, INT, P]
+    lib.dsc_lowrank_bwd_noalloc.restype = INT
+    U64 = ctypes.c_uint64
+    lib.dsc_lowrank_fwd_selftest_timeout.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, I64,
+                                                     INT, INT, U64, P]
+    lib.dsc_lowrank_fwd_selftest_timeout.restype = INT
+    lib.dsc_lowrank_bwd_selftest_timeout.argtypes = [P, P, P, P, P, P, P, P, SZ, I64, I64, I64,
+                                                     I64, I64, I64, INT, INT, U64, P]
+    lib.dsc_lowrank_bwd_selftest_timeout.restype = INT
     lib.dsc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), INT]
     lib.dsc_device_error.restype = INT
     for f in ("dsc_headwise_fwd", "dsc_headwise_bwd", "dsc_lowrank_fwd", "dsc_lowrank_bwd"):
@@ -139,36 +155,111 @@ def _bt_c(x):
 
 
 # --------------------------------------------------- the C entry points ------
+# Each _m_<entry> returns the ctypes argument tuple of that C entry point.
 
-def dsc_headwise_fwd(x, w, y, H, residual=True, stream=None):
-    """y[b,t,c] = residual*x + sum_k w[b,t,c//H,k] x[b,t-k,c]   (in place into y)."""
+def _m_dsc_headwise_fwd(x, w, y, H, residual=True, stream=None):
     B, T, C = _bt_c(x)
     W = w.shape[-1]
     dt = x.dtype
-    _check(load().dsc_headwise_fwd(_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(y, dt, "y"),
-                                   B, T, C, H, W, int(bool(residual)), _dtype_code(x),
-                                   _stream(stream)), "dsc_headwise_fwd")
+    return (_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(y, dt, "y"), B, T, C, H, W,
+            int(bool(residual)), _dtype_code(x), _stream(stream))
+
+
+def _m_dsc_headwise_bwd(x, w, dy, dx, dw, H, residual=True, stream=None):
+    B, T, C = _bt_c(x)
+    W = w.shape[-1]
+    dt = x.dtype
+    return (_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(dy, dt, "dy"), _ptr(dx, dt, "dx"),
+            _ptr(dw, dt, "dw"), B, T, C, H, W, int(bool(residual)), _dtype_code(x),
+            _stream(stream))
+
+
+def _m_dsc_lowrank_fwd(x, z, U, y, H, W, residual=True, stream=None):
+    B, T, C = _bt_c(x)
+    R = z.shape[-1]
+    dt = x.dtype
+    return (_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"), _ptr(y, dt, "y"),
+            B, T, C, H, W, R, int(bool(residual)), _dtype_code(x), _stream(stream))
+
+
+def _m_dsc_lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, H, W, residual=True, stream=None):
+    B, T, C = _bt_c(x)
+    R = z.shape[-1]
+    dt = x.dtype
+    ws_ptr = _ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    return (_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"), _ptr(dy, dt, "dy"),
+            _ptr(dx, dt, "dx"), _ptr(dz, dt, "dz"), _ptr(dU, dt, "dU"), ws_ptr, ws_bytes,
+            B, T, C, H, W, R, int(bool(residual)), _dtype_code(x), _stream(stream))
+
+
+def _m_dsc_lowrank_bwd_noalloc(x, z, U, dy, dx, dz, dU, H, W, residual=True, stream=None):
+    B, T, C = _bt_c(x)
+    R = z.shape[-1]
+    dt = x.dtype
+    return (_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"), _ptr(dy, dt, "dy"),
+            _ptr(dx, dt, "dx"), _ptr(dz, dt, "dz"), _ptr(dU, dt, "dU"), B, T, C, H, W, R,
+            int(bool(residual)), _dtype_code(x), _stream(stream))
+
+
+def _m_dsc_headwise_decode(x, w, state, y, H, residual=True, stream=None):
+    if x.dim() != 2:
+        raise ValueError("x must be [B, C]")
+    B, C = x.shape
+    W = w.shape[-1]
+    dt = x.dtype
+    sp = _ptr(state, dt, "state") if W > 1 else None
+    return (_ptr(x, dt, "x"), _ptr(w, dt, "w"), sp, _ptr(y, dt, "y"), B, C, H, W,
+            int(bool(residual)), _dtype_code(x), _stream(stream))
+
+
+def _m_dsc_lowrank_decode(x, z, U, state, y, H, W, residual=True, stream=None):
+    if x.dim() != 2:
+        raise ValueError("x must be [B, C]")
+    B, C = x.shape
+    R = z.shape[-1]
+    dt = x.dtype
+    sp = _ptr(state, dt, "state") if W > 1 else None
+    return (_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"), sp, _ptr(y, dt, "y"),
+            B, C, H, W, R, int(bool(residual)), _dtype_code(x), _stream(stream))
+
+
+def _m_dsc_static_fwd(x, w, y, residual=True, stream=None):
+    B, T, C = _bt_c(x)
+    W = w.shape[-1]
+    dt = x.dtype
+    return (_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(y, dt, "y"), B, T, C, W,
+            int(bool(residual)), _dtype_code(x), _stream(stream))
+
+
+def _m_dsc_static_bwd(x, w, dy, dx, dw, workspace, residual=True, stream=None):
+    B, T, C = _bt_c(x)
+    W = w.shape[-1]
+    dt = x.dtype
+    ws_ptr = _ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    return (_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(dy, dt, "dy"), _ptr(dx, dt, "dx"),
+            _ptr(dw, dt, "dw"), ws_ptr, ws_bytes, B, T, C, W, int(bool(residual)),
+            _dtype_code(x), _stream(stream))
+
+
+def _call(name, args):
+    _check(getattr(load(), name)(*args), name)
+
+
+def dsc_headwise_fwd(x, w, y, H, residual=True, stream=None):
+    """y[b,t,c] = residual*x + sum_k w[b,t,c//H,k] x[b,t-k,c]   (in place into y)."""
+    _call("dsc_headwise_fwd", _m_dsc_headwise_fwd(x, w, y, H, residual, stream))
 
 
 def dsc_headwise_bwd(x, w, dy, dx, dw, H, residual=True, stream=None):
     """dx, dw of the head-wise DSC (written in place)."""
-    B, T, C = _bt_c(x)
-    W = w.shape[-1]
-    dt = x.dtype
-    _check(load().dsc_headwise_bwd(_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(dy, dt, "dy"),
-                                   _ptr(dx, dt, "dx"), _ptr(dw, dt, "dw"), B, T, C, H, W,
-                                   int(bool(residual)), _dtype_code(x), _stream(stream)),
-           "dsc_headwise_bwd")
+    _call("dsc_headwise_bwd", _m_dsc_headwise_bwd(x, w, dy, dx, dw, H, residual, stream))
 
 
 def dsc_lowrank_fwd(x, z, U, y, H, W, residual=True, stream=None):
     """y of the low-rank fused DSC (filters z_t U formed on-chip)."""
-    B, T, C = _bt_c(x)
-    R = z.shape[-1]
-    dt = x.dtype
-    _check(load().dsc_lowrank_fwd(_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"),
-                                  _ptr(y, dt, "y"), B, T, C, H, W, R, int(bool(residual)),
-                                  _dtype_code(x), _stream(stream)), "dsc_lowrank_fwd")
+    _call("dsc_lowrank_fwd", _m_dsc_lowrank_fwd(x, z, U, y, H, W, residual, stream))
 
 
 def dsc_lowrank_bwd_workspace_size(B, T, C, H, W, R, dtype) -> int:
@@ -177,53 +268,31 @@ def dsc_lowrank_bwd_workspace_size(B, T, C, H, W, R, dtype) -> int:
 
 def dsc_lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, H, W, residual=True, stream=None):
     """dx, dz, dU of the low-rank fused DSC; `workspace` is a uint8 CUDA tensor."""
-    B, T, C = _bt_c(x)
-    R = z.shape[-1]
-    dt = x.dtype
-    ws_ptr = _ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
-    ws_bytes = workspace.numel() if workspace is not None else 0
-    _check(load().dsc_lowrank_bwd(_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"),
-                                  _ptr(dy, dt, "dy"), _ptr(dx, dt, "dx"), _ptr(dz, dt, "dz"),
-                                  _ptr(dU, dt, "dU"), ws_ptr, ws_bytes, B, T, C, H, W, R,
-                                  int(bool(residual)), _dtype_code(x), _stream(stream)),
-           "dsc_lowrank_bwd")
+    _call("dsc_lowrank_bwd",
+          _m_dsc_lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, H, W, residual, stream))
+
+
+def dsc_lowrank_bwd_noalloc(x, z, U, dy, dx, dz, dU, H, W, residual=True, stream=None):
+    """dsc_lowrank_bwd with the library's own fixed scratch (no workspace)."""
+    _call("dsc_lowrank_bwd_noalloc",
+          _m_dsc_lowrank_bwd_noalloc(x, z, U, dy, dx, dz, dU, H, W, residual, stream))
 
 
 def dsc_headwise_decode(x, w, state, y, H, residual=True, stream=None):
     """One decode step: y [B,C] from x [B,C], w [B,G,W] and state [B,W-1,C]
     (updated in place to hold the last W-1 inputs, newest first)."""
-    if x.dim() != 2:
-        raise ValueError("x must be [B, C]")
-    B, C = x.shape
-    W = w.shape[-1]
-    dt = x.dtype
-    sp = _ptr(state, dt, "state") if W > 1 else None
-    _check(load().dsc_headwise_decode(_ptr(x, dt, "x"), _ptr(w, dt, "w"), sp, _ptr(y, dt, "y"),
-                                      B, C, H, W, int(bool(residual)), _dtype_code(x),
-                                      _stream(stream)), "dsc_headwise_decode")
+    _call("dsc_headwise_decode", _m_dsc_headwise_decode(x, w, state, y, H, residual, stream))
 
 
 def dsc_lowrank_decode(x, z, U, state, y, H, W, residual=True, stream=None):
     """Low-rank decode step: taps z [B,R] U formed in fp32, then as above."""
-    if x.dim() != 2:
-        raise ValueError("x must be [B, C]")
-    B, C = x.shape
-    R = z.shape[-1]
-    dt = x.dtype
-    sp = _ptr(state, dt, "state") if W > 1 else None
-    _check(load().dsc_lowrank_decode(_ptr(x, dt, "x"), _ptr(z, dt, "z"), _ptr(U, dt, "U"), sp,
-                                     _ptr(y, dt, "y"), B, C, H, W, R, int(bool(residual)),
-                                     _dtype_code(x), _stream(stream)), "dsc_lowrank_decode")
+    _call("dsc_lowrank_decode",
+          _m_dsc_lowrank_decode(x, z, U, state, y, H, W, residual, stream))
 
 
 def dsc_static_fwd(x, w, y, residual=True, stream=None):
     """Static short conv: y[b,t,c] = residual*x + sum_k w[c,k] x[b,t-k,c]; w is [C, W]."""
-    B, T, C = _bt_c(x)
-    W = w.shape[-1]
-    dt = x.dtype
-    _check(load().dsc_static_fwd(_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(y, dt, "y"),
-                                 B, T, C, W, int(bool(residual)), _dtype_code(x),
-                                 _stream(stream)), "dsc_static_fwd")
+    _call("dsc_static_fwd", _m_dsc_static_fwd(x, w, y, residual, stream))
 
 
 def dsc_static_bwd_workspace_size(B, T, C, W, dtype) -> int:
@@ -232,15 +301,55 @@ def dsc_static_bwd_workspace_size(B, T, C, W, dtype) -> int:
 
 def dsc_static_bwd(x, w, dy, dx, dw, workspace, residual=True, stream=None):
     """dx [B,T,C] and dw [C,W] of the static short conv; `workspace` is a uint8 CUDA tensor."""
-    B, T, C = _bt_c(x)
-    W = w.shape[-1]
-    dt = x.dtype
-    ws_ptr = _ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
-    ws_bytes = workspace.numel() if workspace is not None else 0
-    _check(load().dsc_static_bwd(_ptr(x, dt, "x"), _ptr(w, dt, "w"), _ptr(dy, dt, "dy"),
-                                 _ptr(dx, dt, "dx"), _ptr(dw, dt, "dw"), ws_ptr, ws_bytes,
-                                 B, T, C, W, int(bool(residual)), _dtype_code(x),
-                                 _stream(stream)), "dsc_static_bwd")
+    _call("dsc_static_bwd", _m_dsc_static_bwd(x, w, dy, dx, dw, workspace, residual, stream))
+
+
+def dsc_lowrank_fwd_selftest_timeout(x, z, U, y, H, W, wait_limit_ns, residual=True,
+                                     stream=None):
+    """Failure-path self-test of the tensor-core forward: every bounded wait
+    limited to wait_limit_ns and no loads issued, so the waits run out; read
+    the code with dsc_device_error() afterwards.  y is left unspecified."""
+    a = _m_dsc_lowrank_fwd(x, z, U, y, H, W, residual, stream)
+    _call("dsc_lowrank_fwd_selftest_timeout", a[:-1] + (int(wait_limit_ns), a[-1]))
+
+
+def dsc_lowrank_bwd_selftest_timeout(x, z, U, dy, dx, dz, dU, workspace, H, W, wait_limit_ns,
+                                     residual=True, stream=None):
+    """Failure-path self-test of the tensor-core backward (as above)."""
+    a = _m_dsc_lowrank_bwd(x, z, U, dy, dx, dz, dU, workspace, H, W, residual, stream)
+    _call("dsc_lowrank_bwd_selftest_timeout", a[:-1] + (int(wait_limit_ns), a[-1]))
+
+
+class BoundCall:
+    """One C entry point with its argument tuple marshalled once.
+
+    Calling it issues the same C call again (same pointers, sizes and
+    stream) and raises DSCError on a status other than DSC_OK.  The tensors
+    it was bound to must stay alive and unmoved while it is used."""
+
+    __slots__ = ("name", "fn", "args", "keep")
+
+    def __init__(self, name, args, keep):
+        self.name = name
+        self.fn = getattr(load(), name)
+        self.args = args
+        self.keep = keep          # the bound tensors, kept alive
+
+    def __call__(self):
+        rc = self.fn(*self.args)
+        if rc != DSC_OK:
+            raise DSCError(rc, self.name)
+
+
+def bind(entry, *args, **kw):
+    """Marshal the arguments of C entry point `entry` (e.g. "dsc_lowrank_bwd",
+    same arguments as the Python function of that name) once; return a
+    BoundCall that re-issues the call."""
+    m = globals().get("_m_" + entry)
+    if m is None:
+        raise ValueError(f"no entry point {entry!r}")
+    keep = [a for a in list(args) + list(kw.values()) if isinstance(a, torch.Tensor)]
+    return BoundCall(entry, m(*args, **kw), keep)
 
 
 # ------------------------------------------------------- conveniences --------
