@@ -240,6 +240,37 @@ int dsc_headwise_uses_tma(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
 dsc_status_t dsc_device_error(unsigned int* code, int reset);
 
 /*
+ * Self-tests of the failure path of the tensor-core low-rank kernels
+ * (diagnostic; not for the hot path).  Every wait of those kernels on an
+ * mbarrier is bounded: after a time limit it gives up, records a code in the
+ * device error word (dsc_device_error), lets the CTA's copies and MMAs in
+ * flight finish, frees the CTA's TMEM and returns, so a broken pipeline
+ * ends with an error status instead of hanging the GPU.  These entry points
+ * run dsc_lowrank_fwd / dsc_lowrank_bwd with every limit set to
+ * wait_limit_ns (1 us .. 1 s; the normal limit is 1 s) and with a producer
+ * that issues no loads, so the waits of the other roles run out.  Expected
+ * result: the call enqueues and returns DSC_OK, the kernels end within a
+ * few limits, dsc_device_error then reports a nonzero code (2, 3 or 5), the
+ * outputs are unspecified, and the next normal call on the device runs
+ * correctly.  Arguments as for dsc_lowrank_fwd / dsc_lowrank_bwd, plus
+ * wait_limit_ns; DSC_ERR_UNSUPPORTED when the arguments do not take the
+ * tensor-core path (dsc_lowrank_uses_tensor_cores), DSC_ERR_INVALID_ARG
+ * for an empty problem or a limit outside the range.  Nothing faults or
+ * traps: the waits simply run out.
+ */
+dsc_status_t dsc_lowrank_fwd_selftest_timeout(const void* x, const void* z,
+                                              const void* U, void* y, int64_t B,
+                                              int64_t T, int64_t C, int64_t H,
+                                              int64_t W, int64_t R, int residual,
+                                              dsc_dtype_t dtype,
+                                              uint64_t wait_limit_ns, void* stream);
+dsc_status_t dsc_lowrank_bwd_selftest_timeout(
+    const void* x, const void* z, const void* U, const void* dy, void* dx,
+    void* dz, void* dU, void* workspace, size_t workspace_bytes, int64_t B,
+    int64_t T, int64_t C, int64_t H, int64_t W, int64_t R, int residual,
+    dsc_dtype_t dtype, uint64_t wait_limit_ns, void* stream);
+
+/*
  * Largest workspace dsc_lowrank_bwd_noalloc can provide: 32 MiB.
  */
 #define DSC_LOWRANK_BWD_NOALLOC_MAX_BYTES ((size_t)32 << 20)
@@ -260,7 +291,10 @@ dsc_status_t dsc_device_error(unsigned int* code, int reset);
  *   before anything is enqueued; use dsc_lowrank_bwd for it.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any
- *   stream capture.  The stream must belong to the current device.
+ *   stream capture.  The stream must belong to the current device.  The
+ *   address is kept for the life of the process: after cudaDeviceReset (or
+ *   anything else that destroys and recreates the device's primary context)
+ *   this entry point must not be called again on that device.
  *   All calls share the one array: two calls whose work overlaps on the GPU
  *   (different streams, or different host threads, without ordering between
  *   them) race on it and give wrong results.  Calls ordered on one stream

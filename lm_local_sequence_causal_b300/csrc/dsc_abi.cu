@@ -230,6 +230,45 @@ dsc_status_t dsc_device_error(unsigned int* code, int reset) {
   return from_cuda(e);
 }
 
+dsc_status_t dsc_lowrank_fwd_selftest_timeout(const void* x, const void* z, const void* U,
+                                              void* y, int64_t B, int64_t T, int64_t C,
+                                              int64_t H, int64_t W, int64_t R, int residual,
+                                              dsc_dtype_t dtype, uint64_t wait_limit_ns,
+                                              void* stream) {
+  dsc_status_t st = check_shape(B, T, C, H, W, R, dtype, true);
+  if (st != DSC_OK) return st;
+  if (B * T == 0 || wait_limit_ns < 1000 || wait_limit_ns > 1000000000ull)
+    return DSC_ERR_INVALID_ARG;
+  const Shape s = make_shape(B, T, C, H, W, R, residual, dtype);
+  if (!dsc::lowrank_supported(s) || !dsc::lowrank_tc_supported(s)) return DSC_ERR_UNSUPPORTED;
+  if ((st = check_ptrs({x, z, U, y})) != DSC_OK) return st;
+  if (x == y) return DSC_ERR_INVALID_ARG;
+  return from_cuda(
+      dsc::lowrank_fwd_tc_selftest(x, z, U, y, s, wait_limit_ns, (cudaStream_t)stream));
+}
+
+dsc_status_t dsc_lowrank_bwd_selftest_timeout(const void* x, const void* z, const void* U,
+                                              const void* dy, void* dx, void* dz, void* dU,
+                                              void* workspace, size_t workspace_bytes,
+                                              int64_t B, int64_t T, int64_t C, int64_t H,
+                                              int64_t W, int64_t R, int residual,
+                                              dsc_dtype_t dtype, uint64_t wait_limit_ns,
+                                              void* stream) {
+  dsc_status_t st = check_shape(B, T, C, H, W, R, dtype, true);
+  if (st != DSC_OK) return st;
+  if (B * T == 0 || wait_limit_ns < 1000 || wait_limit_ns > 1000000000ull)
+    return DSC_ERR_INVALID_ARG;
+  const Shape s = make_shape(B, T, C, H, W, R, residual, dtype);
+  if (!dsc::lowrank_supported(s) || !dsc::lowrank_bwd_tc_supported(s)) return DSC_ERR_UNSUPPORTED;
+  if ((st = check_ptrs({x, z, U, dy, dx, dz, dU})) != DSC_OK) return st;
+  if (dx == x || dx == dy || dz == z || dU == U) return DSC_ERR_INVALID_ARG;
+  const size_t need = dsc::lowrank_bwd_tc_workspace(s);
+  if (workspace == nullptr || workspace_bytes < need) return DSC_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return DSC_ERR_ALIGNMENT;
+  return from_cuda(dsc::lowrank_bwd_tc_selftest(x, z, U, dy, dx, dz, dU, workspace, s,
+                                                wait_limit_ns, (cudaStream_t)stream));
+}
+
 int dsc_headwise_uses_tma(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
                           dsc_dtype_t dtype) {
   if (check_shape(B, T, C, H, W, 0, dtype, false) != DSC_OK) return -1;

@@ -74,6 +74,15 @@ cudaError_t lowrank_bwd_tc(const void* x, const void* z, const void* U, const vo
 // Device error word of the tensor-core kernels (0 = no error; otherwise the
 // code of the bounded wait that gave up).  Synchronous; diagnostic only.
 cudaError_t lowrank_tc_error(unsigned int* out, bool reset);
+// Self-test of the failure path: the same kernels with every bounded wait
+// limited to wait_ns and a producer that issues no loads, so the waits of
+// the other roles run out; the kernels record a code in the error word, free
+// their TMEM and return.  Outputs are left unspecified.
+cudaError_t lowrank_fwd_tc_selftest(const void* x, const void* z, const void* U, void* y,
+                                    const Shape& s, uint64_t wait_ns, cudaStream_t st);
+cudaError_t lowrank_bwd_tc_selftest(const void* x, const void* z, const void* U, const void* dy,
+                                    void* dx, void* dz, void* dU, void* ws, const Shape& s,
+                                    uint64_t wait_ns, cudaStream_t st);
 
 // Host helpers (tmap.cu).
 // 3-D tensor map over a dense row-major [d2][d1][d0] tensor of bf16 or fp32,

@@ -33,10 +33,11 @@
 //               swizzled reads, no bank conflicts), forms
 //               y = res*x + sum_k w_k x[t-k] in fp32, rounds once to bf16 and
 //               writes a staged y tile that one thread stores with TMA.
-// The U columns of the CTA's chunks are placed in shared memory once, in the
-// K-major 32-byte-swizzled layout the MMA reads.  Work items are handed out
-// as contiguous ranges, chunk-major, and the grid is at least the number of
-// chunks, so a CTA meets at most two chunks.
+// Each stage also carries the chunk's U columns, loaded by TMA straight from
+// U's natural [R, C*W] layout (MN-major operand, 128-byte swizzle).  Work
+// items are handed out round-robin (item i to CTA i mod grid) in tile-major
+// order, so the CTAs working side by side read neighbouring 128-byte pieces
+// of the same rows of x.
 //
 // Every mbarrier wait is bounded (sm100.cuh); on a timeout the kernel
 // records a code in the device error word, lets its in-flight copies land,
@@ -158,7 +159,8 @@ template <int W, int KS, int HP>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
           const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_y,
-          int ntiles, int nbt, int nchunks, int residual, int hshift) {
+          int ntiles, int nbt, int nchunks, int residual, int hshift, uint64_t wns,
+          int withhold) {
   using L = FwdLayout<W, KS, HP>;
   const int ucols = (CC >> hshift) * W;      // U columns of one chunk (H = 2^hshift)
   extern __shared__ unsigned char smem_raw[];
@@ -211,10 +213,10 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();   // z and U are re-read by many items
       int it = 0;
-      for (; it < nmine; ++it) {
+      for (; it < nmine && !withhold; ++it) {
         const int s = it % NST;
         const uint32_t ph = (it / NST) & 1;
-        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_tc_error, 1)) break;
+        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_tc_error, 1, wns)) break;
         const Item itm = decode_tm(blockIdx.x + static_cast<long long>(it) * gridDim.x,
                                    nchunks, ntiles);
         const uint32_t full = bar_full + 8 * s;
@@ -244,8 +246,8 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const uint32_t ph = (it / NST) & 1;
         const int a = it & 1;
         const uint32_t aph = (it >> 1) & 1;
-        if (!mbar_wait(bar_acce + 8 * a, aph ^ 1, abort_flag, &g_tc_error, 2)) break;
-        if (!mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_tc_error, 2)) break;
+        if (!mbar_wait(bar_acce + 8 * a, aph ^ 1, abort_flag, &g_tc_error, 2, wns)) break;
+        if (!mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_tc_error, 2, wns)) break;
         tc_fence_after();
         const uint32_t st = sb + s * L::STAGE;
         const uint32_t d = tmem + a * 256;
@@ -282,9 +284,9 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       }
       // Every lane waits; the warp leaves together if any wait gave up, so
       // the .sync.aligned TMEM loads below always run converged.
-      bool ok = mbar_wait(bar_yfree + 8 * g, aph, abort_flag, &g_tc_error, 3) &&
-                mbar_wait(bar_accf + 8 * g, aph, abort_flag, &g_tc_error, 3) &&
-                mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_tc_error, 3);
+      bool ok = mbar_wait(bar_yfree + 8 * g, aph, abort_flag, &g_tc_error, 3, wns) &&
+                mbar_wait(bar_accf + 8 * g, aph, abort_flag, &g_tc_error, 3, wns) &&
+                mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_tc_error, 3, wns);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t xt = sb + s * L::STAGE;
@@ -325,7 +327,7 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       }
       // On a failed wait the store is skipped; the abort flag is up, so the
       // whole warp leaves at the next item's waits.
-      if (storer && mbar_wait(bar_yfull + 8 * g, aph, abort_flag, &g_tc_error, 4)) {
+      if (storer && mbar_wait(bar_yfull + 8 * g, aph, abort_flag, &g_tc_error, 4, wns)) {
         const Item itm = decode_tm(blockIdx.x + static_cast<long long>(it) * gridDim.x,
                                    nchunks, ntiles);
         tma_store_3d(&tm_y, ybuf, itm.chunk * CC, itm.t0, itm.b, pol_y);
@@ -394,14 +396,18 @@ struct BwdLayout {
   static constexpr int UBYTES = W * UTAP;                 // U tiles of one chunk
   static constexpr int UALLOC = round1k(UBYTES);
   static constexpr int DWTAP = BM * 128;                  // one tap of dw (16 KB)
+  // Staged dx: for each warp of the dx group and each D part, one box of
+  // 32 tokens x 16 channels (32-byte rows, 32-byte swizzle) that the warp
+  // stores with TMA itself.
+  static constexpr int DXBOX = 32 * 32;
   static constexpr int STG_OFF = 0;
   static constexpr int U_OFF = NSTB * STAGE;
   static constexpr int DW_OFF = U_OFF + 2 * UALLOC;
   static constexpr int DX_OFF = DW_OFF + NT * DWTAP;
-  static constexpr int BAR_OFF = DX_OFF + BM * 128;
+  static constexpr int BAR_OFF = DX_OFF + NEPI * kDParts * DXBOX;
   // full[3] empty[3] dfull[P] dempty[P] dwfull[2] dwfree[2] ufull[2] ufree[2]
-  // uafull[2] uaempty[2] dzfull yfull yfree  (P = kDParts)
-  static constexpr int NBAR = 2 * NSTB + 2 * kDParts + 4 + 8 + 3;
+  // uafull[2] uaempty[2] dzfull  (P = kDParts)
+  static constexpr int NBAR = 2 * NSTB + 2 * kDParts + 4 + 8 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int TOTAL = MISC_OFF + 16 + 1024;
   static constexpr uint32_t TX = 2 * XBOX + ZBOX;
@@ -412,11 +418,15 @@ struct BwdLayout {
 };
 
 struct BwdArgs {
-  __nv_bfloat16* dx;       // [B][T][C]
   float* dz_part;          // [S][B*T][RP]
   float* dU_part;          // [P][RP][C*W]
   const unsigned char* uimg;  // [nchunks][W][RP rows][128 B] swizzled U tiles
   int T, C, ntiles, nchunks, S, P, ntl, residual;
+  // Bounded waits give up after wait_ns; withhold != 0 makes the producer
+  // issue no loads at all, so every wait of the other roles runs out (the
+  // self-test of the failure path; 0 in normal use).
+  unsigned long long wait_ns;
+  int withhold;
 };
 
 template <int W, int RK>
@@ -431,6 +441,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   unsigned char* smem = align1k(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t wns = args.wait_ns;
 
   // This CTA's channel slice [ch0, ch1) and token-tile split [tl0, tl1).
   const int slice = blockIdx.x % args.S, split = blockIdx.x / args.S;
@@ -454,8 +465,6 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   const uint32_t bar_uafull = bar_ufree + 16;
   const uint32_t bar_uaempty = bar_uafull + 16;
   const uint32_t bar_dzfull = bar_uaempty + 16;
-  const uint32_t bar_yfull = bar_dzfull + 8;
-  const uint32_t bar_yfree = bar_yfull + 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF + 4);
 
@@ -479,8 +488,6 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       mbar_init(bar_uaempty + 8 * a, NEPI);
     }
     mbar_init(bar_dzfull, 1);
-    mbar_init(bar_yfull, NEPI);     // (unused: dx is stored from registers)
-    mbar_init(bar_yfree, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_x);
@@ -497,6 +504,12 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The setup above touches no global memory.  From here on the kernel reads
+  // its inputs and writes its outputs, so it waits for the kernels it depends
+  // on (a no-op unless launched as a programmatic dependent), and lets the
+  // reduction kernel that follows it be scheduled.
+  griddep_wait();
+  griddep_launch_dependents();
 
   // item n -> (local chunk lc = n / ntile, local tile lt = n % ntile)
   if (warp == 0) {
@@ -505,11 +518,12 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();
       int n = 0;
-      for (; n < nitems; ++n) {
+      for (; n < nitems && !args.withhold; ++n) {
         const int lc = n / ntile, lt = n - lc * ntile;
         if (lt == 0) {
           const int ub = lc & 1;
-          if (!mbar_wait(bar_ufree + 8 * ub, ((lc >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 1))
+          if (!mbar_wait(bar_ufree + 8 * ub, ((lc >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 1,
+                         wns))
             break;
           const uint32_t uf = bar_ufull + 8 * ub;
           mbar_expect_tx(uf, L::UBYTES);
@@ -522,7 +536,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         }
         const int s = n % NST_;
         const uint32_t ph = (n / NST_) & 1;
-        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_tc_error, 1)) break;
+        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_tc_error, 1, wns)) break;
         const int gt = tl0 + lt;
         const int b = gt / args.ntiles, t0 = (gt - b * args.ntiles) * BM;
         const int c0 = (ch0 + lc) * CC;
@@ -559,14 +573,15 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int lc = n / ntile, lt = n - lc * ntile;
         const int s = n % NST_;
         if (lt == 0)
-          ok = mbar_wait(bar_ufull + 8 * (lc & 1), (lc >> 1) & 1, abort_flag, &g_tc_error, 2);
-        ok = ok && mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 2);
+          ok = mbar_wait(bar_ufull + 8 * (lc & 1), (lc >> 1) & 1, abort_flag, &g_tc_error, 2,
+                         wns);
+        ok = ok && mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 2, wns);
         if (!ok) break;
         const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
         const uint32_t ut = sb + L::U_OFF + (lc & 1) * L::UALLOC;
 #pragma unroll
         for (int hh = 0; hh < kDParts; ++hh) {
-          ok = mbar_wait(bar_dempty + 8 * hh, (n & 1) ^ 1, abort_flag, &g_tc_error, 2);
+          ok = mbar_wait(bar_dempty + 8 * hh, (n & 1) ^ 1, abort_flag, &g_tc_error, 2, wns);
           if (!ok) break;
           tc_fence_after();
           // Part hh = channels PW*hh .. +PW-1: columns k*64 + PW*hh of D, and
@@ -606,19 +621,19 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int s = m % NST_;
         const int ub = lc & 1;
         if (lt == 0) {
-          ok = mbar_wait(bar_ufull + 8 * ub, (lc >> 1) & 1, abort_flag, &g_tc_error, 5);
+          ok = mbar_wait(bar_ufull + 8 * ub, (lc >> 1) & 1, abort_flag, &g_tc_error, 5, wns);
           if (lc >= 2)
             ok = ok && mbar_wait(bar_uaempty + 8 * ub, ((lc >> 1) & 1) ^ 1, abort_flag,
-                                 &g_tc_error, 5);
+                                 &g_tc_error, 5, wns);
         }
-        ok = ok && mbar_wait(bar_full + 8 * s, (m / NST_) & 1, abort_flag, &g_tc_error, 5);
+        ok = ok && mbar_wait(bar_full + 8 * s, (m / NST_) & 1, abort_flag, &g_tc_error, 5, wns);
         if (!ok) break;
         const uint32_t dw = sb + L::DW_OFF;
         const uint32_t ut = sb + L::U_OFF + ub * L::UALLOC;
         const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
 #pragma unroll
         for (int pr = 0; pr < L::NT / 2; ++pr) {
-          ok = mbar_wait(bar_dwfull + 8 * pr, m & 1, abort_flag, &g_tc_error, 5);
+          ok = mbar_wait(bar_dwfull + 8 * pr, m & 1, abort_flag, &g_tc_error, 5, wns);
           if (!ok) break;
           tc_fence_after();
           // Two accumulation chains, interleaved so that consecutive MMAs
@@ -672,9 +687,13 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     if (dx_group) {
       // dx[t] = res*dy[t] + sum_k D_k[t] dy[t+k]: each thread reads dy rows
       // t .. t+W-1 from the staged tile (the 128-byte swizzle keeps the 32
-      // rows of a warp's read conflict-free; measured as fast as passing
-      // rows between lanes by shuffles).  dx goes straight from registers to
-      // global memory.
+      // rows of a warp's read conflict-free).  Per D part a warp owns 32
+      // tokens x 16 channels: it loads their W taps from TMEM in one go and
+      // hands the part back to the MMA issuer at once, then writes dx into
+      // its own 1 KB staging box, which it stores with TMA.
+      const int wd = warp - 2;                              // 0..7 within the group
+      const uint32_t dxst = sb + L::DX_OFF + wd * kDParts * L::DXBOX;
+      const uint64_t pol_dx = policy_evict_first();
       for (int n = 0; n < nitems; ++n) {
         const int lc = n / ntile, lt = n - lc * ntile;
         const int s = n % NST_;
@@ -682,53 +701,73 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int b = gt / args.ntiles, t0 = (gt - b * args.ntiles) * BM;
         const int c0 = (ch0 + lc) * CC;
         const uint32_t dyt = sb + L::STG_OFF + s * L::STAGE + L::XBYTES;
-        ok = mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3);
+        ok = mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3, wns);
         if (!__all_sync(0xffffffffu, ok)) break;
-        const bool row_ok = t0 + tl < args.T;
-        __nv_bfloat16* dxrow = args.dx + (static_cast<int64_t>(b) * args.T + t0 + tl) * args.C + c0;
-        // The channel parts of D in turn; in each, the warp's lane group
-        // takes its tokens and the warp pair splits the part's channels.
-        constexpr int PPC = CC / kDParts / 16;   // 8-channel pieces per warp and part
+        // The warp's box of a part: tokens t0 + 32*lg .. +31, channels
+        // c0 + 32*hh + 16*h .. +15 (two 8-channel pieces).
+        constexpr int PPC = CC / kDParts / 16;
+        const bool box_in = t0 + 32 * lg < args.T;
 #pragma unroll 1
         for (int hh = 0; hh < kDParts; ++hh) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_dfull + 8 * hh, n & 1, abort_flag, &g_tc_error, 3));
-        if (!ok) break;
-        tc_fence_after();
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_dfull + 8 * hh, n & 1, abort_flag,
+                                                 &g_tc_error, 3, wns));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t dk[PPC][W][8];
 #pragma unroll
-        for (int q = 0; q < PPC; ++q) {
-          const int cch = 2 * PPC * hh + PPC * h + q;
-          uint32_t dk[W][8];
+          for (int q = 0; q < PPC; ++q)
 #pragma unroll
-          for (int k = 0; k < W; ++k)
-            tmem_ld8(tmem + tlane + L::TM_D + k * 64 + 8 * cch, dk[k]);
-          uint4 gr[W];
-          gr[0] = lds128(dyt + sw128_offset(tl, cch));
-#pragma unroll
-          for (int k = 1; k < W; ++k) gr[k] = lds128(dyt + sw128_offset(tl + k, cch));
+            for (int k = 0; k < W; ++k)
+              tmem_ld8(tmem + tlane + L::TM_D + k * 64 + 8 * (2 * PPC * hh + PPC * h + q),
+                       dk[q][k]);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < W; ++k) tmem_regs_ready<8>(dk[k]);
-          float2 o[4];
-          const uint32_t g0[4] = {gr[0].x, gr[0].y, gr[0].z, gr[0].w};
+          for (int q = 0; q < PPC; ++q)
 #pragma unroll
-          for (int p = 0; p < 4; ++p) o[p] = args.residual ? bf2f(g0[p]) : make_float2(0.f, 0.f);
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            const uint32_t gw[4] = {gr[k].x, gr[k].y, gr[k].z, gr[k].w};
-#pragma unroll
-            for (int p = 0; p < 4; ++p)
-              o[p] = __ffma2_rn(f2(dk[k][2 * p], dk[k][2 * p + 1]), bf2f(gw[p]), o[p]);
+            for (int k = 0; k < W; ++k) tmem_regs_ready<8>(dk[q][k]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar_dempty + 8 * hh);
+            bulk_wait_read<1>();          // this box's previous store has read it
           }
-          if (row_ok && c0 + 8 * cch < args.C)
-            stcs16(dxrow + 8 * cch, make_uint4(f2bf(o[0]), f2bf(o[1]), f2bf(o[2]), f2bf(o[3])));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_dempty + 8 * hh);
+          __syncwarp();
+          const uint32_t box = dxst + hh * L::DXBOX;
+#pragma unroll
+          for (int q = 0; q < PPC; ++q) {
+            const int cch = 2 * PPC * hh + PPC * h + q;
+            float2 o[4];
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+              const uint4 g = lds128(dyt + sw128_offset(tl + k, cch));
+              const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+              if (k == 0) {
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                  o[p] = args.residual ? bf2f(gw[p]) : make_float2(0.f, 0.f);
+              }
+#pragma unroll
+              for (int p = 0; p < 4; ++p)
+                o[p] = __ffma2_rn(f2(dk[q][k][2 * p], dk[q][k][2 * p + 1]), bf2f(gw[p]), o[p]);
+            }
+            sts128(box + sw32_offset(lane, 8 * q),
+                   make_uint4(f2bf(o[0]), f2bf(o[1]), f2bf(o[2]), f2bf(o[3])));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int cbox = c0 + 32 * hh + 16 * h;
+          if (lane == 0) {
+            // Boxes wholly past C or T are skipped; partly outside ones are
+            // clipped by the tensor map.
+            if (box_in && cbox < args.C)
+              tma_store_3d(&tm_dx, box, cbox, t0 + 32 * lg, b, pol_dx);
+            bulk_commit();
+          }
         }
         if (!ok) break;
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
       }
+      if (lane == 0) bulk_wait<0>();
     } else {
       // dw[t,c,k] = dy[t,c] x[t-k,c].  Thread (chunk wc of 8 channels, run of
       // 4 tokens) keeps a window of x rows in registers, so each x and dy row
@@ -743,7 +782,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int s = n % NST_;
         const int c0 = (ch0 + lc) * CC;
         const uint32_t xt = sb + L::STG_OFF + s * L::STAGE, dyt = xt + L::XBYTES;
-        ok = mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3);
+        ok = mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3, wns);
         if (!__all_sync(0xffffffffu, ok)) break;
         // x box row r holds token t0 - (W-1) + r; token r0 + i needs rows
         // r0 + i + (W-1) - k.
@@ -755,7 +794,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         for (int i = 0; i < 4; ++i) gw[i] = lds128(dyt + sw128_offset(r0 + i, wc));
 #pragma unroll
         for (int pr = 0; pr < L::NT / 2; ++pr) {
-          ok = mbar_wait(bar_dwfree + 8 * pr, (n & 1) ^ 1, abort_flag, &g_tc_error, 3);
+          ok = mbar_wait(bar_dwfree + 8 * pr, (n & 1) ^ 1, abort_flag, &g_tc_error, 3, wns);
           if (!__all_sync(0xffffffffu, ok)) break;
 #pragma unroll
           for (int k = 2 * pr; k < 2 * pr + 2; ++k) {
@@ -782,7 +821,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         // End of a chunk: read out its dU^T accumulator (TMEM lanes = columns).
         if (lt == ntile - 1) {
           const int ub = lc & 1;
-          ok = mbar_wait(bar_uafull + 8 * ub, (lc >> 1) & 1, abort_flag, &g_tc_error, 3);
+          ok = mbar_wait(bar_uafull + 8 * ub, (lc >> 1) & 1, abort_flag, &g_tc_error, 3, wns);
           if (!__all_sync(0xffffffffu, ok)) break;
           tc_fence_after();
           if (h < L::NT / 2) {
@@ -810,7 +849,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       }
       // The dz accumulators of every tile of the split.
       if (ok && nitems > 0) {
-        ok = mbar_wait(bar_dzfull, 0, abort_flag, &g_tc_error, 3);
+        ok = mbar_wait(bar_dzfull, 0, abort_flag, &g_tc_error, 3, wns);
         if (__all_sync(0xffffffffu, ok)) {
           tc_fence_after();
           for (int lt = h; lt < ntile; lt += 2) {
@@ -857,6 +896,9 @@ template <int W, int RK>
 __global__ void lr_u_image(const __nv_bfloat16* __restrict__ U, unsigned char* __restrict__ img,
                            int C, int H, int R, int nchunks) {
   constexpr int RP = 16 * RK;
+  // The backward kernel launched after this one waits for it to complete
+  // before it reads the image; it may be scheduled at once.
+  griddep_launch_dependents();
   const int64_t GW = static_cast<int64_t>(C / H) * W;
   const int total = nchunks * W * RP * 8;              // 16-byte pieces
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -889,6 +931,7 @@ __global__ void lr_u_image(const __nv_bfloat16* __restrict__ U, unsigned char* _
 __global__ void lr_reduce_tc(const float* __restrict__ dz_part, const float* __restrict__ dU_part,
                              __nv_bfloat16* __restrict__ dz, __nv_bfloat16* __restrict__ dU,
                              int64_t nz4, int S, int64_t nU4, int P, int R, int RP, int64_t CW) {
+  griddep_wait();        // the partial sums of the backward kernel launched before this one
   const int64_t total = nz4 + nU4;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -953,9 +996,35 @@ __global__ void lr_reduce_du_tied(const float* __restrict__ dU_part,
 // ------------------------------------------------------------------ host ----
 
 
+// Wait limit of the bounded waits and the self-test switch (withhold: the
+// producer issues no loads, so every other role's wait runs out).
+struct Diag {
+  uint64_t wait_ns = kWaitLimitNs;
+  int withhold = 0;
+};
+
+// Launch as a programmatic dependent of the previous kernel in the stream:
+// it may be scheduled before that kernel ends and waits for it in
+// griddep_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int W, int KS, int HP>
 cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, const Shape& s,
-                       cudaStream_t st) {
+                       cudaStream_t st, const Diag& dg) {
   using L = FwdLayout<W, KS, HP>;
   CUtensorMap tx, tz, tu, ty;
   if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, BM + W - 1, 128) ||
@@ -975,7 +1044,7 @@ cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, con
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kFwdThreads, L::TOTAL, st>>>(
       tx, tz, tu, ty, ntiles, static_cast<int>(nbt), nchunks, s.residual,
-      __builtin_ctzll(static_cast<unsigned long long>(s.H)));
+      __builtin_ctzll(static_cast<unsigned long long>(s.H)), dg.wait_ns, dg.withhold);
   return cudaGetLastError();
 }
 
@@ -1046,7 +1115,7 @@ TcBwdPlan plan_bwd_tc(const Shape& s, int nsm) {
 template <int W, int RK>
 cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* dy, void* dx,
                        void* dz, void* dU, void* ws, const Shape& s, const TcBwdPlan& p,
-                       cudaStream_t st) {
+                       cudaStream_t st, const Diag& dg) {
   using L = BwdLayout<W, RK>;
   CUtensorMap tx, tdy, tz, tdx;
   // z [B][T][R] seen as [B][R/8 groups][T][8]: group g of token t at byte
@@ -1058,12 +1127,11 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
   const uint32_t zb[4] = {8, static_cast<uint32_t>(L::XROWS), static_cast<uint32_t>(L::RP / 8), 1};
   if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
       !make_tmap_3d(&tdy, dy, true, s.C, s.T, s.B, CC, L::XROWS, 128) ||
-      !make_tmap_3d(&tdx, dx, true, s.C, s.T, s.B, CC, BM, 128) ||
+      !make_tmap_3d(&tdx, dx, true, s.C, s.T, s.B, 16, 32, 32) ||
       !make_tmap_4d_bf16(&tz, z, zd, zs, zb))
     return cudaErrorInvalidValue;
   unsigned char* base = static_cast<unsigned char*>(ws);
   BwdArgs a;
-  a.dx = static_cast<__nv_bfloat16*>(dx);
   a.dz_part = reinterpret_cast<float*>(base + p.dz_off);
   a.dU_part = reinterpret_cast<float*>(base + p.dU_off);
   a.uimg = base + p.img_off;
@@ -1075,6 +1143,8 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
   a.P = p.P;
   a.ntl = p.ntl;
   a.residual = s.residual;
+  a.wait_ns = dg.wait_ns;
+  a.withhold = dg.withhold;
   {
     const int pieces = p.nchunks * W * L::RP * 8;
     lr_u_image<W, RK><<<std::min(1184, (pieces + 255) / 256), 256, 0, st>>>(
@@ -1087,17 +1157,17 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
   auto kern = lr_bwd_tc<W, RK>;
   cudaError_t e = set_smem<L>(kern, L::TOTAL);
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(p.S * p.P), kBwdThreads, L::TOTAL, st>>>(tx, tdy, tz, tdx, a);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, static_cast<unsigned>(p.S * p.P), kBwdThreads, L::TOTAL, st, tx, tdy, tz,
+                 tdx, a);
   if (e != cudaSuccess) return e;
   // Per-channel dU partials reduce straight to dU when H = 1; tied filters
   // add their H channels in a second small kernel.
   const int64_t nz4 = s.B * s.T * L::RP / 4, nU4 = s.H == 1 ? s.R * s.C * s.W / 4 : 0;
   const int blocks = static_cast<int>(std::min<int64_t>((nz4 + nU4 + 255) / 256, 148 * 8));
-  lr_reduce_tc<<<blocks, 256, 0, st>>>(a.dz_part, a.dU_part, static_cast<__nv_bfloat16*>(dz),
-                                       static_cast<__nv_bfloat16*>(dU), nz4, p.S, nU4, p.P,
-                                       static_cast<int>(s.R), L::RP, s.C * s.W);
-  e = cudaGetLastError();
+  e = launch_pdl(lr_reduce_tc, static_cast<unsigned>(blocks), 256u, 0, st,
+                 static_cast<const float*>(a.dz_part), static_cast<const float*>(a.dU_part),
+                 static_cast<__nv_bfloat16*>(dz), static_cast<__nv_bfloat16*>(dU), nz4, p.S, nU4,
+                 p.P, static_cast<int>(s.R), static_cast<int>(L::RP), s.C * s.W);
   if (e != cudaSuccess || s.H == 1) return e;
   const int64_t GW = s.G() * s.W;
   const int tb = static_cast<int>(std::min<int64_t>((s.R * GW + 255) / 256, 148 * 8));
@@ -1109,23 +1179,45 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
 
 template <int KS, int HP>
 cudaError_t fwd_hp(const void* x, const void* z, const void* U, void* y, const Shape& s,
-                   cudaStream_t st) {
+                   cudaStream_t st, const Diag& dg) {
   switch (s.W) {
-    case 1: return launch_fwd<1, KS, HP>(x, z, U, y, s, st);
-    case 2: return launch_fwd<2, KS, HP>(x, z, U, y, s, st);
-    case 3: return launch_fwd<3, KS, HP>(x, z, U, y, s, st);
-    default: return launch_fwd<4, KS, HP>(x, z, U, y, s, st);
+    case 1: return launch_fwd<1, KS, HP>(x, z, U, y, s, st, dg);
+    case 2: return launch_fwd<2, KS, HP>(x, z, U, y, s, st, dg);
+    case 3: return launch_fwd<3, KS, HP>(x, z, U, y, s, st, dg);
+    default: return launch_fwd<4, KS, HP>(x, z, U, y, s, st, dg);
   }
 }
 
 template <int KS>
 cudaError_t fwd_w(const void* x, const void* z, const void* U, void* y, const Shape& s, int hp,
-                  cudaStream_t st) {
+                  cudaStream_t st, const Diag& dg) {
   switch (hp) {
-    case 1: return fwd_hp<KS, 1>(x, z, U, y, s, st);
-    case 2: return fwd_hp<KS, 2>(x, z, U, y, s, st);
-    case 4: return fwd_hp<KS, 4>(x, z, U, y, s, st);
-    default: return fwd_hp<KS, 8>(x, z, U, y, s, st);
+    case 1: return fwd_hp<KS, 1>(x, z, U, y, s, st, dg);
+    case 2: return fwd_hp<KS, 2>(x, z, U, y, s, st, dg);
+    case 4: return fwd_hp<KS, 4>(x, z, U, y, s, st, dg);
+    default: return fwd_hp<KS, 8>(x, z, U, y, s, st, dg);
+  }
+}
+
+cudaError_t bwd_dispatch(const void* x, const void* z, const void* U, const void* dy, void* dx,
+                         void* dz, void* dU, void* ws, const Shape& s, cudaStream_t st,
+                         const Diag& dg) {
+  const int nsm = sm_count();
+  if (nsm <= 0) return cudaErrorNoDevice;
+  const TcBwdPlan p = plan_bwd_tc(s, nsm);
+  if (rk_of(s.R) == 2) {
+    switch (s.W) {
+      case 1: return launch_bwd<1, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+      case 2: return launch_bwd<2, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+      case 3: return launch_bwd<3, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+      default: return launch_bwd<4, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+    }
+  }
+  switch (s.W) {
+    case 1: return launch_bwd<1, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+    case 2: return launch_bwd<2, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+    case 3: return launch_bwd<3, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+    default: return launch_bwd<4, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
   }
 }
 
@@ -1147,23 +1239,17 @@ cudaError_t lowrank_bwd_tc(const void* x, const void* z, const void* U, const vo
                            void* dx, void* dz, void* dU, void* ws, const Shape& s,
                            cudaStream_t st) {
   if (!lowrank_bwd_tc_supported(s)) return cudaErrorNotSupported;
-  const int nsm = sm_count();
-  if (nsm <= 0) return cudaErrorNoDevice;
-  const TcBwdPlan p = plan_bwd_tc(s, nsm);
-  if (rk_of(s.R) == 2) {
-    switch (s.W) {
-      case 1: return launch_bwd<1, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-      case 2: return launch_bwd<2, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-      case 3: return launch_bwd<3, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-      default: return launch_bwd<4, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-    }
-  }
-  switch (s.W) {
-    case 1: return launch_bwd<1, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-    case 2: return launch_bwd<2, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-    case 3: return launch_bwd<3, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-    default: return launch_bwd<4, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st);
-  }
+  return bwd_dispatch(x, z, U, dy, dx, dz, dU, ws, s, st, Diag{});
+}
+
+cudaError_t lowrank_bwd_tc_selftest(const void* x, const void* z, const void* U, const void* dy,
+                                    void* dx, void* dz, void* dU, void* ws, const Shape& s,
+                                    uint64_t wait_ns, cudaStream_t st) {
+  if (!lowrank_bwd_tc_supported(s)) return cudaErrorNotSupported;
+  Diag dg;
+  dg.wait_ns = wait_ns;
+  dg.withhold = 1;
+  return bwd_dispatch(x, z, U, dy, dx, dz, dU, ws, s, st, dg);
 }
 
 // Forward: tied filters need whole groups in a 64-channel chunk and a U
@@ -1178,14 +1264,30 @@ bool lowrank_tc_supported(const Shape& s) {
          s.C < (int64_t(1) << 24);
 }
 
+namespace {
+cudaError_t fwd_dispatch(const void* x, const void* z, const void* U, void* y, const Shape& s,
+                         cudaStream_t st, const Diag& dg) {
+  const int hp = s.H >= 8 ? 8 : static_cast<int>(s.H);
+  switch (s.R > 16 ? 2 : 1) {
+    case 1: return fwd_w<1>(x, z, U, y, s, hp, st, dg);
+    default: return fwd_w<2>(x, z, U, y, s, hp, st, dg);
+  }
+}
+}  // namespace
+
 cudaError_t lowrank_fwd_tc(const void* x, const void* z, const void* U, void* y,
                            const Shape& s, cudaStream_t st) {
   if (!lowrank_tc_supported(s)) return cudaErrorNotSupported;
-  const int hp = s.H >= 8 ? 8 : static_cast<int>(s.H);
-  switch (s.R > 16 ? 2 : 1) {
-    case 1: return fwd_w<1>(x, z, U, y, s, hp, st);
-    default: return fwd_w<2>(x, z, U, y, s, hp, st);
-  }
+  return fwd_dispatch(x, z, U, y, s, st, Diag{});
+}
+
+cudaError_t lowrank_fwd_tc_selftest(const void* x, const void* z, const void* U, void* y,
+                                    const Shape& s, uint64_t wait_ns, cudaStream_t st) {
+  if (!lowrank_tc_supported(s)) return cudaErrorNotSupported;
+  Diag dg;
+  dg.wait_ns = wait_ns;
+  dg.withhold = 1;
+  return fwd_dispatch(x, z, U, y, s, st, dg);
 }
 
 cudaError_t lowrank_tc_error(unsigned int* out, bool reset) {

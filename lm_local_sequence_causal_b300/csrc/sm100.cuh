@@ -63,17 +63,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of parity `parity` to complete.  Returns false if the
-// CTA's abort flag is up or the time limit passed (then it records `code`
-// in *err and raises the abort flag).
+// CTA's abort flag is up or `limit_ns` passed (then it records `code` in
+// *err and raises the abort flag).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* err, unsigned int code) {
+                                          unsigned int* err, unsigned int code,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicCAS(err, 0u, code);
         return false;
@@ -156,6 +157,18 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// Programmatic dependent launch.  griddep_wait() returns once every grid
+// this one depends on has completed and its memory writes are visible (at
+// once for a grid launched without the programmatic-serialization
+// attribute); griddep_launch_dependents() lets the grid launched after this
+// one with that attribute be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Named barrier over `count` threads (a multiple of 32).

@@ -166,3 +166,27 @@ def test_static_validation_and_workspace(lib):
              None) == dsc.DSC_ERR_INVALID_ARG                                   # dx aliases x
     assert g(A, A2, A3, A4, None, None, 0, 0, 8, 64, 4, 1, BF16,
              None) == dsc.DSC_ERR_INVALID_ARG                                   # empty, no dw
+
+
+def test_selftest_entry_points_validate_on_the_host(lib):
+    f = lib.dsc_lowrank_fwd_selftest_timeout
+    u64 = ctypes.c_uint64
+    ok_limit = u64(2_000_000)
+    # limit out of range, empty problem: rejected before any CUDA call
+    for lim in (0, 999, 2_000_000_000):
+        assert f(A, A2, A3, A4, 2, 256, 128, 1, 4, 16, 1, BF16, u64(lim), None) == \
+            dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, A4, 0, 256, 128, 1, 4, 16, 1, BF16, ok_limit, None) == \
+        dsc.DSC_ERR_INVALID_ARG
+    # fp32 and R = 3 take the CUDA-core kernels, which have no self-test
+    assert f(A, A2, A3, A4, 2, 256, 128, 1, 4, 16, 1, F32, ok_limit, None) == \
+        dsc.DSC_ERR_UNSUPPORTED
+    assert f(A, A2, A3, A4, 2, 256, 128, 1, 4, 3, 1, BF16, ok_limit, None) == \
+        dsc.DSC_ERR_UNSUPPORTED
+    assert f(A, MIS, A3, A4, 2, 256, 128, 1, 4, 16, 1, BF16, ok_limit, None) == \
+        dsc.DSC_ERR_ALIGNMENT
+    g = lib.dsc_lowrank_bwd_selftest_timeout
+    assert g(A, A2, A3, A4, A5, P(0x60000), P(0x70000), None, 0, 2, 256, 128, 1, 4, 16, 1,
+             BF16, ok_limit, None) == dsc.DSC_ERR_WORKSPACE
+    assert g(A, A2, A3, A4, A5, P(0x60000), P(0x70000), P(0x80000), 1 << 30, 2, 256, 128, 1, 4,
+             16, 1, BF16, u64(10), None) == dsc.DSC_ERR_INVALID_ARG
