@@ -24,15 +24,15 @@
 //               (M = 128, N = 64*W, K = 16 per instruction) into one of two
 //               TMEM accumulators and commits them to mbarriers.
 //   warps 2-17  epilogue, two groups of 8 warps taking alternate items (each
-//               with its own TMEM accumulator and y staging buffer, so the
-//               groups overlap); in a group, warp (w % 4) owns TMEM lanes
-//               32*(w % 4) .. +31 = those tokens and the two warps of each
-//               lane group split the chunk's channels.  Each thread loads its token's
-//               W taps for 8 channels at a time (tcgen05.ld), reads
-//               x[t-k] for the same 8 channels from the staged tile (16-byte
-//               swizzled reads, no bank conflicts), forms
-//               y = res*x + sum_k w_k x[t-k] in fp32, rounds once to bf16 and
-//               writes a staged y tile that one thread stores with TMA.
+//               with its own TMEM accumulator, so the groups overlap); in a
+//               group, warp (w % 4) owns TMEM lanes 32*(w % 4) .. +31 = those
+//               tokens and the two warps of each lane group split the
+//               chunk's channels.  Each thread loads its token's W taps for
+//               8 channels at a time (tcgen05.ld), reads x[t-k] for the same
+//               8 channels from the staged tile (16-byte swizzled reads, no
+//               bank conflicts), forms y = res*x + sum_k w_k x[t-k] in fp32,
+//               rounds once to bf16 and writes the warp's own staging box
+//               (32 tokens x 32 channels), which the warp stores with TMA.
 // Each stage also carries the chunk's U columns, loaded by TMA straight from
 // U's natural [R, C*W] layout (MN-major operand, 128-byte swizzle).  Work
 // items are handed out round-robin (item i to CTA i mod grid) in tile-major
@@ -76,7 +76,7 @@ constexpr int NEPI = 8;     // warps per backward epilogue group (4 lane groups 
 // producer, D-MMA issuer, dx group, dw group, dz/dU-MMA issuer
 constexpr int kBwdThreads = (3 + 2 * NEPI) * 32;
 constexpr int kDzduWarp = 2 + 2 * NEPI;
-// The backward's D accumulator is formed and handed to the dx warps in
+// The dx warps read the backward's D accumulator and hand it back in
 // kDParts channel parts of 64 / kDParts channels each.
 constexpr int kDParts = 2;
 constexpr uint32_t kTmemCols = 512;
@@ -97,15 +97,23 @@ struct FwdLayout {
   static constexpr int UATOM = KS * 16 * 128;         // 64 U columns x R rows (2 or 4 KB)
   static constexpr int UBYTES = NA * UATOM;
   static constexpr int STAGE = XBYTES + KS * ZBYTES + round1k(UBYTES);
-  static constexpr int YBYTES = BM * 128;             // staged y tile of one group
+  // Staged y: every epilogue warp has its own box(es) of 32 tokens x 32
+  // channels (64-byte rows, 64-byte swizzle) that it stores with TMA; two
+  // per warp where shared memory allows, so a warp never waits for its
+  // previous store to be read.
+  static constexpr int YBOX = 32 * 64;
   static constexpr int Z_IN = XBYTES;                 // offsets inside a stage
   static constexpr int U_IN = XBYTES + KS * ZBYTES;
   static constexpr int Y_OFF = NST * STAGE;
-  static constexpr int BAR_OFF = Y_OFF + 2 * YBYTES;
-  // full[NST] empty[NST] accf[2] acce[2] yfull[2] yfree[2]
-  static constexpr int NBAR = 2 * NST + 8;
+  // full[NST] empty[NST] accf[2] acce[2]
+  static constexpr int NBAR = 2 * NST + 4;
+  static constexpr int total(int nyb) {
+    return Y_OFF + NEPI_F * nyb * YBOX + NBAR * 8 + 16 + 1024;   // + slack to align the base
+  }
+  static constexpr int NYB = total(2) <= 227 * 1024 ? 2 : 1;
+  static constexpr int BAR_OFF = Y_OFF + NEPI_F * NYB * YBOX;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int TOTAL = MISC_OFF + 16 + 1024;  // + slack to align the base
+  static constexpr int TOTAL = MISC_OFF + 16 + 1024;
   static constexpr uint32_t TX = XBOX + KS * ZBYTES + UBYTES;  // bytes landing per stage
 };
 
@@ -133,6 +141,14 @@ __device__ __forceinline__ float2 f2(uint32_t lo, uint32_t hi) {
 __device__ __forceinline__ float2 bf2f(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
+// Byte offset of the 16-byte chunk `chunk` (0..3) of row `row` in a tile
+// with 64-byte rows stored by TMA with SWIZZLE_64B (address bits 4-5 XORed
+// with bits 7-8; the tile 512-byte aligned).
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t chunk) {
+  const uint32_t o = row * 64u + chunk * 16u;
+  return o ^ ((o >> 3) & 0x30u);
+}
+
 __device__ __forceinline__ uint32_t f2bf(float2 v) {
   __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -160,7 +176,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
           const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_y,
           int ntiles, int nbt, int nchunks, int residual, int hshift, uint64_t wns,
-          int withhold) {
+          int withhold, int C, int T) {
   using L = FwdLayout<W, KS, HP>;
   const int ucols = (CC >> hshift) * W;      // U columns of one chunk (H = 2^hshift)
   extern __shared__ unsigned char smem_raw[];
@@ -178,8 +194,6 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   const uint32_t bar_empty = bar_full + NST * 8;
   const uint32_t bar_accf = bar_empty + NST * 8;
   const uint32_t bar_acce = bar_accf + 16;
-  const uint32_t bar_yfull = bar_acce + 16;
-  const uint32_t bar_yfree = bar_yfull + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF + 4);
 
@@ -191,8 +205,6 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_accf + 8 * a, 1);
       mbar_init(bar_acce + 8 * a, NGRP);
-      mbar_init(bar_yfull + 8 * a, NGRP);
-      mbar_init(bar_yfree + 8 * a, 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -264,32 +276,33 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   } else {
     // --------------------------------------------------------- epilogue --
     // Two independent groups of 8 warps: group g takes the items it with
-    // it % 2 == g, using TMEM accumulator g and y staging buffer g, so one
-    // group's loads, math and store overlap the other group's.
+    // it % 2 == g, using TMEM accumulator g, so one group's loads, math and
+    // stores overlap the other group's.  A warp owns 32 tokens (its TMEM
+    // lanes) and 32 channels (four 8-channel pieces) of the item and stores
+    // them itself from its staging box, so no group-wide barrier sits on
+    // the output path; the accumulator is handed back right after the
+    // warp's last TMEM load.
     const int g = (warp - 2) >> 3;
     const int lg = warp & 3;                 // TMEM lane group of this warp
     const int h = ((warp - 2) >> 2) & 1;     // channel half of the chunk
     const int tl = lg * 32 + lane;           // token within the tile
-    const bool storer = ((warp - 2) & 7) == 0 && lane == 0;
     const uint64_t pol_y = policy_evict_first();
     const uint32_t tbase = tmem + (static_cast<uint32_t>(lg * 32) << 16) + g * 256;
-    const uint32_t ybuf = sb + L::Y_OFF + g * L::YBYTES;
+    const uint32_t ybase = sb + L::Y_OFF + (warp - 2) * L::NYB * L::YBOX;
     for (int it = g; it < nmine; it += 2) {
       const int s = it % NST;
       const uint32_t ph = (it / NST) & 1;
       const uint32_t aph = (it >> 1) & 1;
-      if (storer) {
-        bulk_wait_read<0>();                 // this group's previous store has read the buffer
-        mbar_arrive(bar_yfree + 8 * g);
-      }
       // Every lane waits; the warp leaves together if any wait gave up, so
       // the .sync.aligned TMEM loads below always run converged.
-      bool ok = mbar_wait(bar_yfree + 8 * g, aph, abort_flag, &g_tc_error, 3, wns) &&
-                mbar_wait(bar_accf + 8 * g, aph, abort_flag, &g_tc_error, 3, wns) &&
+      bool ok = mbar_wait(bar_accf + 8 * g, aph, abort_flag, &g_tc_error, 3, wns) &&
                 mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_tc_error, 3, wns);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t xt = sb + s * L::STAGE;
+      const uint32_t ybuf = ybase + ((it >> 1) % L::NYB) * L::YBOX;
+      if (lane == 0) bulk_wait_read<L::NYB - 1>();   // this box's previous store has read it
+      __syncwarp();
       // Four 8-channel pieces per warp; tap k of the chunk's filter group gl
       // is column gl*W + k, and channel c of the chunk uses group c / H.
       constexpr int NCP = 8 / HP * W;        // TMEM columns of one piece
@@ -300,41 +313,47 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         // first filter group of the piece: cch*8/H (H = HP below 8)
         const int g0 = HP < 8 ? cch * 8 / HP : (cch * 8) >> hshift;
         tmem_ld_cols<NCP>(tbase + g0 * W, acc);
-        float xv[W][8];
+        uint4 xr[W];
 #pragma unroll
-        for (int k = 0; k < W; ++k)
-          unpack16<__nv_bfloat16>(lds128(xt + sw128_offset(tl + (W - 1) - k, cch)), xv[k]);
+        for (int k = 0; k < W; ++k) xr[k] = lds128(xt + sw128_offset(tl + (W - 1) - k, cch));
         tmem_wait_ld();
-        tmem_regs_ready<8 * W>(acc);
-        float out[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float v = residual ? xv[0][c] : 0.f;
-#pragma unroll
-          for (int k = 0; k < W; ++k)
-            v = fmaf(__uint_as_float(acc[(c / HP) * W + k]), xv[k][c], v);
-          out[c] = v;
+        tmem_regs_ready<NCP>(acc);
+        if (q == 3) {                         // the accumulator is in registers
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acce + 8 * g);
         }
-        sts128(ybuf + sw128_offset(tl, cch), pack16<__nv_bfloat16>(out));
+        float2 o[4];
+        const uint32_t x0[4] = {xr[0].x, xr[0].y, xr[0].z, xr[0].w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) o[p] = residual ? bf2f(x0[p]) : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const uint32_t xw[4] = {xr[k].x, xr[k].y, xr[k].z, xr[k].w};
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            // channels 2p, 2p+1 of the piece use filter groups (2p)/HP, (2p+1)/HP
+            const float2 wk = f2(acc[((2 * p) / HP) * W + k], acc[((2 * p + 1) / HP) * W + k]);
+            o[p] = __ffma2_rn(wk, bf2f(xw[p]), o[p]);
+          }
+        }
+        sts128(ybuf + sw64_offset(lane, q),
+               make_uint4(f2bf(o[0]), f2bf(o[1]), f2bf(o[2]), f2bf(o[3])));
       }
-      tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar_acce + 8 * g);
         mbar_arrive(bar_empty + 8 * s);
-        mbar_arrive(bar_yfull + 8 * g);
-      }
-      // On a failed wait the store is skipped; the abort flag is up, so the
-      // whole warp leaves at the next item's waits.
-      if (storer && mbar_wait(bar_yfull + 8 * g, aph, abort_flag, &g_tc_error, 4, wns)) {
         const Item itm = decode_tm(blockIdx.x + static_cast<long long>(it) * gridDim.x,
                                    nchunks, ntiles);
-        tma_store_3d(&tm_y, ybuf, itm.chunk * CC, itm.t0, itm.b, pol_y);
+        const int cbox = itm.chunk * CC + 32 * h, tbox = itm.t0 + 32 * lg;
+        // Boxes wholly past C or T are skipped; partly outside ones are
+        // clipped by the tensor map.
+        if (cbox < C && tbox < T) tma_store_3d(&tm_y, ybuf, cbox, tbox, itm.b, pol_y);
         bulk_commit();
       }
     }
-    if (storer) bulk_wait<0>();
+    if (lane == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
@@ -560,12 +579,12 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     }
   } else if (warp == 1) {
     // --------------------------------------------------- D-MMA issuer --
-    // D_k for every item in kDParts channel parts (N = 64 / kDParts), each
-    // as soon as the dx group has freed that part: the first part of item
-    // n+1 is formed while the dx group works on the last part of item n.
+    // D_k for every item: one MMA of N = 64 (the chunk's channels) per tap
+    // and K-step, A = z K-major (shifted k rows), B = U MN-major.  The dx
+    // group hands D back in kDParts channel parts, each right after loading
+    // it into registers, so the next item's D is formed while the dx group
+    // still computes on the current one.
     if (lane == 0) {
-      constexpr int PW = CC / kDParts;                        // channels of a part
-      constexpr uint32_t id_d = idesc_major(BM, PW, 0, 1);    // A z K-major, B U MN-major
       const uint32_t zsbo = L::XROWS * 16;                    // stride of the two z halves
       int issued[kDParts] = {};
       bool ok = true;
@@ -579,24 +598,32 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         if (!ok) break;
         const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
         const uint32_t ut = sb + L::U_OFF + (lc & 1) * L::UALLOC;
+        // Descriptor bases; every operand below starts a multiple of 16
+        // bytes further, which is that many units added to the start field
+        // (shared-memory addresses stay below 256 KB, so it cannot carry).
+        const uint64_t zd0 = make_desc(zt, zsbo, 128, 0);
+        const uint64_t ud0 = make_desc(ut, 16, 1024, 2);
+        // Once every part is free; every part is signalled on completion.
 #pragma unroll
-        for (int hh = 0; hh < kDParts; ++hh) {
-          ok = mbar_wait(bar_dempty + 8 * hh, (n & 1) ^ 1, abort_flag, &g_tc_error, 2, wns);
-          if (!ok) break;
-          tc_fence_after();
-          // Part hh = channels PW*hh .. +PW-1: columns k*64 + PW*hh of D, and
-          // U columns PW*hh .. of the chunk's tiles (2*PW*hh bytes into each
-          // 128-byte swizzled row).
+        for (int hh = 0; hh < kDParts; ++hh)
+          ok = ok && mbar_wait(bar_dempty + 8 * hh, (n & 1) ^ 1, abort_flag, &g_tc_error, 2, wns);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          constexpr uint32_t id_d64 = idesc_major(BM, CC, 0, 1);
 #pragma unroll
           for (int k = 0; k < W; ++k)
 #pragma unroll
             for (int ks = 0; ks < RK; ++ks)
-              mma_bf16(tmem + L::TM_D + k * 64 + PW * hh,
-                       make_desc(zt + 16 * k + 2 * ks * zsbo, zsbo, 128, 0),
-                       make_desc(ut + k * L::UTAP + ks * 2048 + 2 * PW * hh, 16, 1024, 2), id_d,
-                       ks > 0 ? 1u : 0u);
-          mma_commit(bar_dfull + 8 * hh);
-          ++issued[hh];
+              mma_bf16(tmem + L::TM_D + k * 64,
+                       zd0 + static_cast<uint64_t>((16 * k + 2 * ks * zsbo) >> 4),
+                       ud0 + static_cast<uint64_t>((k * L::UTAP + ks * 2048) >> 4),
+                       id_d64, ks > 0 ? 1u : 0u);
+#pragma unroll
+          for (int hh = 0; hh < kDParts; ++hh) {
+            mma_commit(bar_dfull + 8 * hh);
+            ++issued[hh];
+          }
         }
         if (!ok) break;
         mma_commit(bar_empty + 8 * s);
@@ -631,6 +658,13 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const uint32_t dw = sb + L::DW_OFF;
         const uint32_t ut = sb + L::U_OFF + ub * L::UALLOC;
         const uint32_t zt = sb + L::STG_OFF + s * L::STAGE + 2 * L::XBYTES;
+        // Descriptor bases (offsets below are multiples of 16 bytes, added to
+        // the start field as for the D MMAs).
+        const uint64_t dza = make_desc(dw, 16, 1024, 2), dzb = make_desc(ut, 16, 1024, 2);
+        const uint64_t dua = make_desc(dw, L::DWTAP, 1024, 2), dub = make_desc(zt, 128, zsbo, 0);
+        const uint32_t tdz = tmem + L::TM_DZ + lt * RP;
+        const uint32_t tdu = tmem + L::TM_DU + ub * (L::NT / 2) * RP;
+        const uint32_t first_dz = lc > 0 ? 1u : 0u, first_du = lt > 0 ? 1u : 0u;
 #pragma unroll
         for (int pr = 0; pr < L::NT / 2; ++pr) {
           ok = mbar_wait(bar_dwfull + 8 * pr, m & 1, abort_flag, &g_tc_error, 5, wns);
@@ -645,14 +679,12 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             const int q = 8 * pr + i;
             const int k = q >> 2, cb = q & 3;
             if (k < W)
-              mma_bf16(tmem + L::TM_DZ + lt * RP,
-                       make_desc(dw + k * L::DWTAP + cb * 32, 16, 1024, 2),
-                       make_desc(ut + k * L::UTAP + cb * 32, 16, 1024, 2), id_dz,
-                       (lc > 0 || q > 0) ? 1u : 0u);
-            mma_bf16(tmem + L::TM_DU + ub * (L::NT / 2) * RP + pr * RP,
-                     make_desc(dw + 2 * pr * L::DWTAP + i * 2048, L::DWTAP, 1024, 2),
-                     make_desc(zt + i * 256, 128, zsbo, 0), id_du,
-                     (lt > 0 || i > 0) ? 1u : 0u);
+              mma_bf16(tdz, dza + static_cast<uint64_t>((k * L::DWTAP + cb * 32) >> 4),
+                       dzb + static_cast<uint64_t>((k * L::UTAP + cb * 32) >> 4), id_dz,
+                       q > 0 ? 1u : first_dz);
+            mma_bf16(tdu + pr * RP,
+                     dua + static_cast<uint64_t>((2 * pr * L::DWTAP + i * 2048) >> 4),
+                     dub + static_cast<uint64_t>((i * 256) >> 4), id_du, i > 0 ? 1u : first_du);
           }
           mma_commit(bar_dwfree + 8 * pr);
           ++issued_pair[pr];
@@ -1030,7 +1062,7 @@ cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, con
   if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, CC, BM + W - 1, 128) ||
       !make_tmap_3d(&tz, z, true, s.R, s.T, s.B, 16, BM, 32) ||
       !make_tmap_3d(&tu, U, true, s.G() * s.W, s.R, 1, 64, 16 * KS, 128) ||
-      !make_tmap_3d(&ty, y, true, s.C, s.T, s.B, CC, BM, 128))
+      !make_tmap_3d(&ty, y, true, s.C, s.T, s.B, 32, 32, 64))
     return cudaErrorInvalidValue;
   const int ntiles = static_cast<int>((s.T + BM - 1) / BM);
   const int nchunks = static_cast<int>((s.C + CC - 1) / CC);
@@ -1044,7 +1076,8 @@ cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, con
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kFwdThreads, L::TOTAL, st>>>(
       tx, tz, tu, ty, ntiles, static_cast<int>(nbt), nchunks, s.residual,
-      __builtin_ctzll(static_cast<unsigned long long>(s.H)), dg.wait_ns, dg.withhold);
+      __builtin_ctzll(static_cast<unsigned long long>(s.H)), dg.wait_ns, dg.withhold,
+      static_cast<int>(s.C), static_cast<int>(s.T));
   return cudaGetLastError();
 }
 
