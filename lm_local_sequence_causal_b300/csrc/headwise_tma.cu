@@ -55,7 +55,15 @@ template <int W, int H, bool BWD, int CW>
 struct HwLayout {
   static constexpr int NB = CW / 64;                  // 64-channel boxes per item
   static constexpr int GI = CW / H;                   // groups per item
-  static constexpr int WROW = GI * W * 2;             // bytes of one token's taps
+  // PADW: the item's taps (GI*W elements) are not a whole number of 16-byte
+  // units (e.g. 4 groups x 3 taps = 24 bytes), so no TMA box can start at
+  // them.  The box is then 16 elements wide and starts at the 8-element
+  // boundary at or below them: the taps sit 0 or 4 elements into it (GI*W
+  // is a multiple of 4 and at most 12), and dw goes straight from
+  // registers to global memory instead of through a staged TMA store.
+  static constexpr bool PADW = (GI * W * 2) % 16 != 0;
+  static_assert(!PADW || ((GI * W) % 4 == 0 && GI * W <= 12), "padded filter box");
+  static constexpr int WROW = PADW ? 32 : GI * W * 2;  // bytes of one row of the w box
   static constexpr int WSW = (WROW == 32 || WROW == 64) ? WROW : 0;  // swizzle of the w box
   static constexpr int XROWS = BM + W - 1;
   static constexpr int XBOX = XROWS * 128;            // one 64-channel box
@@ -68,7 +76,7 @@ struct HwLayout {
   static constexpr int STAGE = W_IN + WBYTES;
   static constexpr int OBOX = BM * 128;               // one staged 64-channel output box
   static constexpr int OBYTES = NB * OBOX;            // staged y / dx tile of one group
-  static constexpr int DWBYTES = BWD ? round1k(BM * WROW) : 0;  // staged dw tile of one group
+  static constexpr int DWBYTES = (BWD && !PADW) ? round1k(BM * WROW) : 0;  // staged dw tile
   // Shared memory of the layout with `nst` stages.
   static constexpr int total(int nst) {
     return nst * STAGE + 2 * OBYTES + 2 * DWBYTES + (2 * nst + 4) * 8 + 16 + 1024;
@@ -133,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_out,
               const __grid_constant__ CUtensorMap tm_dw, int ntiles, int nbt, int nchunks,
-              int residual) {
+              int residual, __nv_bfloat16* __restrict__ dw_out, int T, int64_t GW) {
   using L = HwLayout<W, H, BWD, CW>;
   constexpr int NST = L::NST;
   constexpr int NB = L::NB;
@@ -168,7 +176,7 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     tma_prefetch_desc(&tm_out);
     if constexpr (BWD) {
       tma_prefetch_desc(&tm_dy);
-      tma_prefetch_desc(&tm_dw);
+      if constexpr (!L::PADW) tma_prefetch_desc(&tm_dw);
     }
   }
   __syncthreads();
@@ -195,7 +203,8 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             tma_load_3d(st + L::DY_IN + j * L::XBYTES, &tm_dy, full, itm.chunk * CW + 64 * j,
                         itm.t0, itm.b, pol);
         }
-        tma_load_3d(st + L::W_IN, &tm_w, full, itm.chunk * L::GI * W, itm.t0, itm.b, pol);
+        const int wx = itm.chunk * L::GI * W;
+        tma_load_3d(st + L::W_IN, &tm_w, full, L::PADW ? (wx & ~7) : wx, itm.t0, itm.b, pol);
       }
       for (int j = std::max(0, it - NST); j < it; ++j)
         drain_wait(bar_full + 8 * (j % NST), (j / NST) & 1);
@@ -222,6 +231,10 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
       if (!__all_sync(0xffffffffu, ok)) break;
       const uint32_t st = sb + s * L::STAGE;
       const uint32_t wt = st + L::W_IN;
+      // PADW: the item's taps start woff elements into the w box.
+      const HwItem itm0 =
+          hw_decode(blockIdx.x + static_cast<long long>(it) * gridDim.x, nchunks, ntiles);
+      const int woff = L::PADW ? (itm0.chunk * L::GI * W) & 7 : 0;
       if constexpr (!BWD) {
         // y = res*x + sum_k w[t,g,k] x[t-k]
 #pragma unroll
@@ -232,7 +245,7 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
           float taps[W];
 #pragma unroll
           for (int k = 0; k < W; ++k)
-            taps[k] = lds_bf16(wt + wtile_offset<L::WROW, L::WSW>(tl, (gl * W + k) * 2));
+            taps[k] = lds_bf16(wt + wtile_offset<L::WROW, L::WSW>(tl, (woff + gl * W + k) * 2));
           float xv[W][8];
 #pragma unroll
           for (int k = 0; k < W; ++k)
@@ -250,6 +263,7 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         }
       } else {
         // dx = res*dy + sum_k w[t+k,g,k] dy[t+k];  dw[t,g,k] = sum_{c in g} dy[t,c] x[t-k,c]
+        [[maybe_unused]] uint32_t dwp[L::PADW ? (PPW * 8 / H) * W / 2 + 1 : 1];
         float p[W];
 #pragma unroll
         for (int k = 0; k < W; ++k) p[k] = 0.f;
@@ -262,7 +276,7 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
           float wk[W];
 #pragma unroll
           for (int k = 0; k < W; ++k)
-            wk[k] = lds_bf16(wt + wtile_offset<L::WROW, L::WSW>(tl + k, (gl * W + k) * 2));
+            wk[k] = lds_bf16(wt + wtile_offset<L::WROW, L::WSW>(tl + k, (woff + gl * W + k) * 2));
           float gv[W][8];
 #pragma unroll
           for (int k = 0; k < W; ++k)
@@ -286,11 +300,42 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
           }
           // The last 8-channel piece of a group: its W taps are complete.
           if (((cch + 1) * 8) % H == 0) {
+            if constexpr (L::PADW) {
+              // bf16 pairs in registers; written below in 4-byte stores.  The
+              // warp's pieces hold whole groups (PPW*8 is a multiple of H),
+              // so the piece's group within the warp is q*8/H.
+              static_assert((PPW * 8) % H == 0, "whole groups per warp");
+              const int gw = ((q * 8) / H) * W;     // first element of the group within the warp
 #pragma unroll
-            for (int k = 0; k < W; ++k) {
-              sts_bf16(dwbuf + wtile_offset<L::WROW, L::WSW>(tl, (gl * W + k) * 2), p[k]);
-              p[k] = 0.f;
+              for (int k = 0; k < W; ++k) {
+                const uint32_t v = __bfloat16_as_ushort(__float2bfloat16_rn(p[k]));
+                const int e = gw + k;
+                if (e & 1) dwp[e >> 1] |= v << 16;
+                else dwp[e >> 1] = v;
+                p[k] = 0.f;
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < W; ++k) {
+                sts_bf16(dwbuf + wtile_offset<L::WROW, L::WSW>(tl, (gl * W + k) * 2), p[k]);
+                p[k] = 0.f;
+              }
             }
+          }
+        }
+        if constexpr (L::PADW) {
+          // The warp's groups are contiguous in dw: (PPW*8/H)*W elements of
+          // 2 bytes starting at a 4-byte multiple (GI*W and the groups
+          // before this warp's are multiples of 4 and 2 elements).
+          constexpr int NE = (PPW * 8 / H) * W;
+          static_assert(NE % 2 == 0, "whole bf16 pairs");
+          const int t = itm0.t0 + tl;
+          if (t < T) {
+            uint32_t* dst = reinterpret_cast<uint32_t*>(
+                dw_out + (static_cast<int64_t>(itm0.b) * T + t) * GW +
+                (static_cast<int64_t>(itm0.chunk) * L::GI + (PPW * h * 8) / H) * W);
+#pragma unroll
+            for (int e = 0; e < NE / 2; ++e) dst[e] = dwp[e];
           }
         }
       }
@@ -306,7 +351,8 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < NB; ++j)
           tma_store_3d(&tm_out, obuf + j * L::OBOX, itm.chunk * CW + 64 * j, itm.t0, itm.b, pol);
-        if constexpr (BWD) tma_store_3d(&tm_dw, dwbuf, itm.chunk * L::GI * W, itm.t0, itm.b, pol);
+        if constexpr (BWD && !L::PADW)
+          tma_store_3d(&tm_dw, dwbuf, itm.chunk * L::GI * W, itm.t0, itm.b, pol);
         bulk_commit();
       }
     }
@@ -322,13 +368,18 @@ cudaError_t launch(const void* x, const void* dy, const void* w, void* out, void
   const uint64_t GW = static_cast<uint64_t>(s.C / H) * W;
   CUtensorMap tx, tdy, tw, tout, tdw;
   if (!make_tmap_3d(&tx, x, true, s.C, s.T, s.B, 64, L::XROWS, 128) ||
-      !make_tmap_3d(&tw, w, true, GW, s.T, s.B, L::GI * W, L::WROWS, L::WSW) ||
+      !make_tmap_3d(&tw, w, true, GW, s.T, s.B, L::WROW / 2, L::WROWS, L::WSW) ||
       !make_tmap_3d(&tout, out, true, s.C, s.T, s.B, 64, BM, 128))
     return cudaErrorInvalidValue;
   if constexpr (BWD) {
-    if (!make_tmap_3d(&tdy, dy, true, s.C, s.T, s.B, 64, L::XROWS, 128) ||
-        !make_tmap_3d(&tdw, dw, true, GW, s.T, s.B, L::GI * W, BM, L::WSW))
+    if (!make_tmap_3d(&tdy, dy, true, s.C, s.T, s.B, 64, L::XROWS, 128))
       return cudaErrorInvalidValue;
+    if constexpr (L::PADW) {
+      tdw = tw;                                 // unused: dw is written from registers
+    } else {
+      if (!make_tmap_3d(&tdw, dw, true, GW, s.T, s.B, L::GI * W, BM, L::WSW))
+        return cudaErrorInvalidValue;
+    }
   } else {
     tdy = tx;
     tdw = tw;
@@ -343,14 +394,11 @@ cudaError_t launch(const void* x, const void* dy, const void* w, void* out, void
   cudaError_t e = set_smem<L>(kern, L::TOTAL);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kThreads, L::TOTAL, st>>>(
-      tx, tdy, tw, tout, tdw, ntiles, static_cast<int>(nbt), nchunks, s.residual);
+      tx, tdy, tw, tout, tdw, ntiles, static_cast<int>(nbt), nchunks, s.residual,
+      static_cast<__nv_bfloat16*>(dw), static_cast<int>(s.T), static_cast<int64_t>(GW));
   return cudaGetLastError();
 }
 
-// The (H, W) pairs whose filter rows make a legal TMA box (a multiple of 16
-// bytes for the item's CW/H groups x W taps), with the narrowest item that
-// does: 64 channels for H = 8 (any W), (16, 2), (16, 4), (32, 4); 128
-// channels for (16, 1), (16, 3), (32, 2), (64, 4).
 // Channel width of the item for (H, W) and C, 0 if there is no TMA path.
 // The pairs are those whose filter rows make a TMA box of a multiple of 16
 // bytes.  The narrowest legal item is 64 channels for H = 8, (16, 2),
@@ -358,16 +406,18 @@ cudaError_t launch(const void* x, const void* dy, const void* w, void* out, void
 // forward of (8, 1), (16, 2) and (32, 4) takes 128-channel items when C
 // allows (measured 3 to 15% faster at C = 6144); for the others, (16, 4)
 // included, the wider item leaves room for only two stages and is slower.
-// The backward of (16, 3) has no TMA path: with 48-byte filter rows its two
-// stages, two staged outputs and two staged dw tiles do not fit shared
-// memory.
+// The backward of (16, 3) takes 64-channel items with the padded filter box
+// (24-byte filter rows; see PADW in the layout): 128-channel items with
+// 48-byte rows do not fit shared memory with two stages.  Its filter tensor
+// rows (3C/16 elements) must still be a multiple of 16 bytes for the tensor
+// map, so C is a multiple of 128.
 int item_width(int64_t H, int64_t W, bool bwd, int64_t C) {
   const bool narrow = (H == 8 && W >= 1 && W <= 4) || (H == 16 && (W == 2 || W == 4)) ||
                       (H == 32 && W == 4);
   const bool wide_only = (H == 16 && (W == 1 || W == 3)) || (H == 32 && W == 2) ||
                          (H == 64 && W == 4);
   const bool wide_fwd = (H == 8 && W == 1) || (H == 16 && W == 2) || (H == 32 && W == 4);
-  if (bwd && H == 16 && W == 3) return 0;
+  if (bwd && H == 16 && W == 3) return C % 128 == 0 ? 64 : 0;
   if (wide_only) return C % 128 == 0 ? 128 : 0;
   if (!narrow) return 0;
   if (!bwd && wide_fwd && C % 128 == 0) return 128;
@@ -384,6 +434,9 @@ cudaError_t dispatch_cw(const void* x, const void* dy, const void* w, void* out,
       case 8 * 8 + 3: return launch<3, 8, BWD, 64>(x, dy, w, out, dw, s, st);
       case 8 * 8 + 4: return launch<4, 8, BWD, 64>(x, dy, w, out, dw, s, st);
       case 16 * 8 + 2: return launch<2, 16, BWD, 64>(x, dy, w, out, dw, s, st);
+      case 16 * 8 + 3:
+        if constexpr (BWD) return launch<3, 16, true, 64>(x, dy, w, out, dw, s, st);
+        break;
       case 16 * 8 + 4: return launch<4, 16, BWD, 64>(x, dy, w, out, dw, s, st);
       case 32 * 8 + 4: return launch<4, 32, BWD, 64>(x, dy, w, out, dw, s, st);
       default: break;

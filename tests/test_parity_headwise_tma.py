@@ -52,11 +52,27 @@ def test_every_legal_group_size_and_width(H, W, CW, residual):
     check(wl, seed=H * 10 + W + 100 * residual)
 
 
-def test_w3_h16_forward_on_tma_backward_streaming():
-    # the all-linear sweep's H = 16, W = 3: forward on TMA, backward on the
-    # register-streaming kernel (its TMA tiles would not fit shared memory)
+def test_w3_h16_on_tma():
+    # the all-linear sweep's H = 16, W = 3: forward on 128-channel items,
+    # backward on 64-channel items with the padded filter box (24-byte
+    # filter rows: the taps start 0 or 4 elements into the loaded box, on
+    # alternate chunks) and dw written from registers
     wl = syn.Workload("hw_tma_w3", B=2, T=300, C=640, W=3, H=16)
-    check(wl, seed=33, paths=1)
+    check(wl, seed=33, paths=3)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 127, 129, 300])
+@pytest.mark.parametrize("residual", [False, True])
+def test_w3_h16_short_ragged_and_three_wide_chunks(T, residual):
+    # six 64-channel backward chunks (both tap offsets, 0 and 4), three
+    # 128-channel forward chunks, short and ragged sequences
+    wl = syn.Workload("hw_tma_w3_T", B=3, T=T, C=384, W=3, H=16, residual=residual)
+    check(wl, seed=T + 7 * residual, paths=3)
+
+
+def test_w3_h16_backward_many_items_per_cta():
+    wl = syn.Workload("hw_tma_w3_multi", B=4, T=2048, C=1024, W=3, H=16, residual=True)
+    check(wl, seed=3, paths=3)
 
 
 def test_linear_rnn_shape_on_tma():
@@ -70,7 +86,7 @@ def test_short_and_ragged_sequences(T):
     check(wl, seed=T)
 
 
-def test_many_items_per_cta():
+def test_many_items_per_cta_qkv_pair():
     wl = syn.Workload("hw_tma_big", B=4, T=1024, C=2048, W=4, H=16)
     check(wl, seed=5)
 
@@ -79,7 +95,9 @@ def test_routing():
     q = dsc.dsc_headwise_uses_tma
     bf = torch.bfloat16
     assert q(8, 2048, 6144, 16, 4, bf) == 3           # the QKV placement
-    assert q(8, 2048, 6144, 16, 3, bf) == 1           # forward only (128-channel items)
+    assert q(8, 2048, 6144, 16, 3, bf) == 3           # fwd 128-ch items, bwd padded box
+    assert q(8, 2048, 6080, 16, 3, bf) == 0           # C % 128 != 0: filter rows 3C/16
+    assert q(8, 2048, 320, 16, 3, bf) == 0            # elements, not 16-byte multiples
     assert q(2, 16384, 4096, 64, 4, bf) == 3          # linear-RNN shape (128-channel items)
     assert q(8, 2048, 6144, 64, 3, bf) == 0           # 6-tap rows: no legal box
     assert q(8, 2048, 6144, 16, 4, torch.float32) == 0
