@@ -119,9 +119,42 @@ __device__ __forceinline__ float lds_bf16(uint32_t addr) {
   return __uint_as_float(static_cast<uint32_t>(v) << 16);
 }
 
+// Two fp32 rounded to nearest-even bf16, packed (first in the low half).
+__device__ __forceinline__ uint32_t f2bf2(float a, float b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+}
+
 __device__ __forceinline__ void sts_bf16(uint32_t addr, float f) {
   const unsigned short v = __bfloat16_as_ushort(__float2bfloat16_rn(f));
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// The W taps of filter group gl in row r of the staged w tile, as fp32.
+// W = 2 or 4 taps are one 4- or 8-byte load (their offset is a multiple of
+// the access size, so it stays inside one 16-byte swizzle unit): threads on
+// consecutive rows then meet at most two to a bank, where W separate 2-byte
+// loads meet eight to a bank on 32-byte rows.
+template <int W, int row, int sw>
+__device__ __forceinline__ void load_taps(uint32_t wt, uint32_t r, int e0, float (&t)[W]) {
+  const uint32_t a = wt + wtile_offset<row, sw>(r, static_cast<uint32_t>(e0) * 2);
+  if constexpr (W == 4) {
+    uint32_t lo, hi;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(a));
+    t[0] = __uint_as_float(lo << 16);
+    t[1] = __uint_as_float(lo & 0xffff0000u);
+    t[2] = __uint_as_float(hi << 16);
+    t[3] = __uint_as_float(hi & 0xffff0000u);
+  } else if constexpr (W == 2) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    t[0] = __uint_as_float(v << 16);
+    t[1] = __uint_as_float(v & 0xffff0000u);
+  } else {
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+      t[k] = lds_bf16(wt + wtile_offset<row, sw>(r, static_cast<uint32_t>(e0 + k) * 2));
+  }
 }
 
 struct HwItem {
@@ -243,9 +276,7 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
           const int gl = cch * 8 / H;            // its filter group within the item
           const uint32_t xt = st + (cch >> 3) * L::XBYTES;
           float taps[W];
-#pragma unroll
-          for (int k = 0; k < W; ++k)
-            taps[k] = lds_bf16(wt + wtile_offset<L::WROW, L::WSW>(tl, (woff + gl * W + k) * 2));
+          load_taps<W, L::WROW, L::WSW>(wt, tl, woff + gl * W, taps);
           float xv[W][8];
 #pragma unroll
           for (int k = 0; k < W; ++k)
@@ -273,10 +304,14 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
           const int gl = cch * 8 / H;
           const uint32_t xt = st + (cch >> 3) * L::XBYTES;
           const uint32_t dyt = st + L::DY_IN + (cch >> 3) * L::XBYTES;
+          // tap k of row tl + k (the filter of token t+k)
           float wk[W];
 #pragma unroll
-          for (int k = 0; k < W; ++k)
-            wk[k] = lds_bf16(wt + wtile_offset<L::WROW, L::WSW>(tl + k, (woff + gl * W + k) * 2));
+          for (int k = 0; k < W; ++k) {
+            float row_taps[W];
+            load_taps<W, L::WROW, L::WSW>(wt, tl + k, woff + gl * W, row_taps);
+            wk[k] = row_taps[k];
+          }
           float gv[W][8];
 #pragma unroll
           for (int k = 0; k < W; ++k)
@@ -314,6 +349,19 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                 else dwp[e >> 1] = v;
                 p[k] = 0.f;
               }
+            } else if constexpr (W == 4 || W == 2) {
+              // the group's taps in one 8- or 4-byte store
+              uint32_t pk[2];
+              pk[0] = f2bf2(p[0], p[1]);
+              if constexpr (W == 4) pk[1] = f2bf2(p[2], p[3]);
+              const uint32_t a = dwbuf + wtile_offset<L::WROW, L::WSW>(tl, (gl * W) * 2);
+              if constexpr (W == 4)
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(pk[0]), "r"(pk[1])
+                             : "memory");
+              else
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(pk[0]) : "memory");
+#pragma unroll
+              for (int k = 0; k < W; ++k) p[k] = 0.f;
             } else {
 #pragma unroll
               for (int k = 0; k < W; ++k) {
