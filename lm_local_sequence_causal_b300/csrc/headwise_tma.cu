@@ -64,6 +64,11 @@ struct HwLayout {
   static constexpr bool PADW = (GI * W * 2) % 16 != 0;
   static_assert(!PADW || ((GI * W) % 4 == 0 && GI * W <= 12), "padded filter box");
   static constexpr int WROW = PADW ? 32 : GI * W * 2;  // bytes of one row of the w box
+  // TOK2 (backward with a group wider than half the item, H = 64 on 64-channel
+  // items): two adjacent lanes share a token, each taking half the item's
+  // channels, so the group's dw is one shuffle away instead of in another warp.
+  static constexpr bool TOK2 = BWD && H > CW / 2;
+  static_assert(!TOK2 || (H == CW && PADW), "two-lane tokens: one group per item");
   static constexpr int WSW = (WROW == 32 || WROW == 64) ? WROW : 0;  // swizzle of the w box
   static constexpr int XROWS = BM + W - 1;
   static constexpr int XBOX = XROWS * 128;            // one 64-channel box
@@ -245,9 +250,12 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
   } else {
     // --------------------------------------------------------- epilogue --
     const int g = (warp - 1) >> 3;             // group: items it with it % 2 == g
+    // The thread's token of the tile (tl) and channel half of the item (h):
+    // a warp owns 32 tokens and one half, or with TOK2 16 tokens, two
+    // adjacent lanes per token.
     const int lg = warp & 3;
-    const int h = ((warp - 1) >> 2) & 1;
-    const int tl = lg * 32 + lane;
+    const int h = L::TOK2 ? (lane & 1) : ((warp - 1) >> 2) & 1;
+    const int tl = L::TOK2 ? ((warp - 1) & 7) * 16 + (lane >> 1) : lg * 32 + lane;
     const bool storer = ((warp - 1) & 7) == 0 && lane == 0;
     const uint64_t pol = policy_evict_first();
     const uint32_t obuf = sb + L::O_OFF + g * L::OBYTES;
@@ -334,8 +342,9 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             for (int c = 0; c < 8; ++c) p[k] = fmaf(gv[0][c], xv[c], p[k]);
           }
           // The last 8-channel piece of a group: its W taps are complete.
-          if (((cch + 1) * 8) % H == 0) {
-            if constexpr (L::PADW) {
+          if (!L::TOK2 && ((cch + 1) * 8) % H == 0) {
+            if constexpr (L::TOK2) {
+            } else if constexpr (L::PADW) {
               // bf16 pairs in registers; written below in 4-byte stores.  The
               // warp's pieces hold whole groups (PPW*8 is a multiple of H),
               // so the piece's group within the warp is q*8/H.
@@ -371,7 +380,21 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             }
           }
         }
-        if constexpr (L::PADW) {
+        if constexpr (L::TOK2) {
+          // The token's two lanes hold the sums over their halves of the
+          // group; the even lane adds them and writes the W taps (8 bytes at
+          // an 8-byte multiple: W = 4 and the group index times 4).
+          static_assert(W == 4, "two-lane tokens are built for W = 4");
+#pragma unroll
+          for (int k = 0; k < W; ++k) p[k] += __shfl_xor_sync(0xffffffffu, p[k], 1);
+          const int t = itm0.t0 + tl;
+          if (h == 0 && t < T) {
+            uint2* dst = reinterpret_cast<uint2*>(
+                dw_out + (static_cast<int64_t>(itm0.b) * T + t) * GW +
+                static_cast<int64_t>(itm0.chunk) * L::GI * W);
+            *dst = make_uint2(f2bf2(p[0], p[1]), f2bf2(p[2], p[3]));
+          }
+        } else if constexpr (L::PADW) {
           // The warp's groups are contiguous in dw: (PPW*8/H)*W elements of
           // 2 bytes starting at a 4-byte multiple (GI*W and the groups
           // before this warp's are multiples of 4 and 2 elements).
@@ -456,7 +479,10 @@ cudaError_t launch(const void* x, const void* dy, const void* w, void* out, void
 // included, the wider item leaves room for only two stages and is slower.
 // The backward of (16, 3) takes 64-channel items with the padded filter box
 // (24-byte filter rows; see PADW in the layout): 128-channel items with
-// 48-byte rows do not fit shared memory with two stages.  Its filter tensor
+// 48-byte rows do not fit shared memory with two stages.  The backward of
+// (64, 4) takes 64-channel items too (one group per item, two lanes per
+// token: TOK2), which leave room for four stages where 128-channel items
+// leave two.  Its filter tensor
 // rows (3C/16 elements) must still be a multiple of 16 bytes for the tensor
 // map, so C is a multiple of 128.
 int item_width(int64_t H, int64_t W, bool bwd, int64_t C) {
@@ -466,6 +492,7 @@ int item_width(int64_t H, int64_t W, bool bwd, int64_t C) {
                          (H == 64 && W == 4);
   const bool wide_fwd = (H == 8 && W == 1) || (H == 16 && W == 2) || (H == 32 && W == 4);
   if (bwd && H == 16 && W == 3) return C % 128 == 0 ? 64 : 0;
+  if (bwd && H == 64 && W == 4) return C % 128 == 0 ? 64 : 0;
   if (wide_only) return C % 128 == 0 ? 128 : 0;
   if (!narrow) return 0;
   if (!bwd && wide_fwd && C % 128 == 0) return 128;
@@ -484,6 +511,9 @@ cudaError_t dispatch_cw(const void* x, const void* dy, const void* w, void* out,
       case 16 * 8 + 2: return launch<2, 16, BWD, 64>(x, dy, w, out, dw, s, st);
       case 16 * 8 + 3:
         if constexpr (BWD) return launch<3, 16, true, 64>(x, dy, w, out, dw, s, st);
+        break;
+      case 64 * 8 + 4:
+        if constexpr (BWD) return launch<4, 64, true, 64>(x, dy, w, out, dw, s, st);
         break;
       case 16 * 8 + 4: return launch<4, 16, BWD, 64>(x, dy, w, out, dw, s, st);
       case 32 * 8 + 4: return launch<4, 32, BWD, 64>(x, dy, w, out, dw, s, st);

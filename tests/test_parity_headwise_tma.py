@@ -75,6 +75,16 @@ def test_w3_h16_backward_many_items_per_cta():
     check(wl, seed=3, paths=3)
 
 
+@pytest.mark.parametrize("T", [1, 2, 129, 300])
+@pytest.mark.parametrize("residual", [False, True])
+def test_h64_backward_two_lanes_per_token(T, residual):
+    # H = 64 backward on 64-channel items: one filter group per item, its dw
+    # summed over two adjacent lanes of a token; six chunks give both filter
+    # box offsets (0 and 4 elements)
+    wl = syn.Workload("hw_tma_h64", B=3, T=T, C=384, W=4, H=64, residual=residual)
+    check(wl, seed=T + 11 * residual, paths=3)
+
+
 def test_linear_rnn_shape_on_tma():
     wl = syn.Workload("hw_tma_rnn", B=1, T=1100, C=512, W=4, H=64, hot_frac=0.05)
     check(wl, seed=64)
