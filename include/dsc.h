@@ -221,10 +221,11 @@ int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H,
  * dsc_headwise_bwd does; a clear bit means the register-streaming kernels.
  * The TMA kernels take bf16 with (H, W) whose filter rows make a 16-byte
  * multiple box: items of 64 channels for H = 8 (any W), (16, 2), (16, 4),
- * (32, 4) and the (16, 3) backward (whose 24-byte filter rows are loaded as
- * a wider aligned box), and of 128 channels for (16, 1), the (16, 3)
- * forward, (32, 2), (64, 4); C must be a multiple of the item width.  -1 if
- * the arguments are invalid.  Host only; touches no device.
+ * (32, 4) and the backward of (16, 3) and (64, 4) (whose filter rows are
+ * loaded as a wider aligned box; C a multiple of 128), and of 128 channels
+ * for (16, 1), the forward of (16, 3) and (64, 4), and (32, 2); C must be a
+ * multiple of the item width.  -1 if the arguments are invalid.  Host only;
+ * touches no device.
  */
 int dsc_headwise_uses_tma(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W,
                           dsc_dtype_t dtype);

@@ -21,8 +21,10 @@
 //               each with its own staged output tiles; in a group the warp
 //               (lane group lg = w % 4, half h) owns tokens 32*lg .. +31 and
 //               half of the chunk's channels (8-channel pieces, which make
-//               whole groups since H >= 8).  Outputs go to staged
-//               tiles that one thread of the group stores with TMA.
+//               whole groups since H >= 8; in the H = 64 backward a warp
+//               owns 16 tokens, two adjacent lanes each, see TOK2).  Outputs
+//               go to staged tiles that one thread of the group stores with
+//               TMA (dw of the padded-box layouts from registers).
 // Every mbarrier wait is bounded (sm100.cuh); a timeout records a code in
 // this file's device error word and the CTA returns.
 #include <cuda_bf16.h>
