@@ -32,6 +32,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -109,6 +110,63 @@ def recorded_traffic(name):
     if not e or e.get("source_sha256_16") != source_hash(KERNEL_SOURCES[name]):
         return None
     return e.get("bytes_per_launch")
+
+
+def entry_of_kernel(name):
+    """The entry point a kernel of this library belongs to, from its ncu name."""
+    m = re.search(r"hw_tma_kernel<\s*\d+,\s*\d+,\s*(\d)", name)
+    if m:
+        return "headwise_bwd" if m.group(1) == "1" else "headwise_fwd"
+    if "lr_fwd_tc" in name:
+        return "lowrank_fwd"
+    if any(k in name for k in ("lr_u_image", "lr_bwd_tc", "lr_reduce_tc")):
+        return "lowrank_bwd"
+    return None
+
+
+def record_traffic(csv_path, command, out_path=None):
+    """Write the per-entry-point DRAM traffic record from an ncu launch list
+    (`--metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum
+    --csv`) of whole bench steps; bytes are per call (summed over the entry
+    point's launches, divided by the number of calls captured)."""
+    import csv
+    with open(csv_path) as fh:
+        lines = [l for l in fh if l.startswith('"')]
+    launches = {}
+    for r in csv.DictReader(lines):
+        e = launches.setdefault(r["ID"], {"name": r["Kernel Name"]})
+        e[r["Metric Name"]] = float(r["Metric Value"])
+    sums, calls = {}, {}
+    for e in launches.values():
+        ent = entry_of_kernel(e["name"])
+        if ent is None:
+            continue
+        s = sums.setdefault(ent, {"read": 0.0, "write": 0.0})
+        s["read"] += e.get("dram__bytes_read.sum", 0.0)
+        s["write"] += e.get("dram__bytes_write.sum", 0.0)
+        main = ("hw_tma_kernel" in e["name"] or "lr_fwd_tc" in e["name"]
+                or "lr_bwd_tc" in e["name"])
+        calls[ent] = calls.get(ent, 0) + (1 if main else 0)
+    out = {"_note": (
+        "DRAM bytes (read + write) per call of each entry point at the QKV size "
+        "(B=8 T=2048 C=6144 W=4 bf16), from one ncu pass over whole bench steps: "
+        f"`{command}`, written by `python3 bench.py --record-traffic <that csv>`. "
+        "Writes still dirty in L2 when a launch ends are counted in later launches. "
+        "An entry is used only while the hash of its kernel source matches.")}
+    for ent in ("headwise_fwd", "headwise_bwd", "lowrank_fwd", "lowrank_bwd"):
+        if ent not in sums or not calls.get(ent):
+            continue
+        n = calls[ent]
+        rd, wr = int(sums[ent]["read"] / n), int(sums[ent]["write"] / n)
+        out[ent] = {"bytes_per_launch": rd + wr, "read": rd, "write": wr,
+                    "source_sha256_16": source_hash(KERNEL_SOURCES[ent])}
+        if ent == "lowrank_bwd":
+            out[ent]["launches"] = "lr_u_image + lr_bwd_tc + lr_reduce_tc"
+    p = out_path or os.path.join(ROOT, "profiles", "dram_traffic.json")
+    with open(p, "w") as fh:
+        json.dump(out, fh, indent=1)
+        fh.write("\n")
+    return out
 
 
 # ------------------------------------------------------------ clocks --------
@@ -683,7 +741,15 @@ def main():
     ap.add_argument("--sweep-only", action="store_true",
                     help="print only the sweep line (single GPU)")
     ap.add_argument("--sweep-calls", type=int, default=20)
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="host only: write profiles/dram_traffic.json from an ncu launch list "
+                         "of whole bench steps, then exit")
+    ap.add_argument("--record-command", default="",
+                    help="the ncu command that produced --record-traffic's CSV (for the note)")
     args = ap.parse_args()
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.record_command), indent=1))
+        return 0
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -186,6 +186,9 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
   constexpr int NST = L::NST;
   constexpr int NB = L::NB;
   constexpr int PPW = CW / 16;                         // 8-channel pieces per warp
+  // A thread's pieces start on a group boundary, so a group's taps can be
+  // loaded at its first piece (with TOK2 the item is one group).
+  static_assert((PPW * 8) % H == 0 || L::TOK2, "pieces start on a group boundary");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align1k(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -279,14 +282,17 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
           hw_decode(blockIdx.x + static_cast<long long>(it) * gridDim.x, nchunks, ntiles);
       const int woff = L::PADW ? (itm0.chunk * L::GI * W) & 7 : 0;
       if constexpr (!BWD) {
-        // y = res*x + sum_k w[t,g,k] x[t-k]
+        // y = res*x + sum_k w[t,g,k] x[t-k].  A group's taps are loaded at
+        // its first piece: a new group starts where 8q is a multiple of H
+        // (the thread's first piece starts one, as 8*PPW is a multiple of H
+        // or the item holds one group).
+        float taps[W];
 #pragma unroll
         for (int q = 0; q < PPW; ++q) {
           const int cch = PPW * h + q;           // 8-channel piece of the item
           const int gl = cch * 8 / H;            // its filter group within the item
           const uint32_t xt = st + (cch >> 3) * L::XBYTES;
-          float taps[W];
-          load_taps<W, L::WROW, L::WSW>(wt, tl, woff + gl * W, taps);
+          if ((q * 8) % H == 0) load_taps<W, L::WROW, L::WSW>(wt, tl, woff + gl * W, taps);
           float xv[W][8];
 #pragma unroll
           for (int k = 0; k < W; ++k)
@@ -308,19 +314,21 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         float p[W];
 #pragma unroll
         for (int k = 0; k < W; ++k) p[k] = 0.f;
+        float wk[W];                             // tap k of row tl + k (the filter of token t+k)
 #pragma unroll
         for (int q = 0; q < PPW; ++q) {
           const int cch = PPW * h + q;
           const int gl = cch * 8 / H;
           const uint32_t xt = st + (cch >> 3) * L::XBYTES;
           const uint32_t dyt = st + L::DY_IN + (cch >> 3) * L::XBYTES;
-          // tap k of row tl + k (the filter of token t+k)
-          float wk[W];
+          // loaded at the group's first piece, as in the forward
+          if ((q * 8) % H == 0) {
 #pragma unroll
-          for (int k = 0; k < W; ++k) {
-            float row_taps[W];
-            load_taps<W, L::WROW, L::WSW>(wt, tl + k, woff + gl * W, row_taps);
-            wk[k] = row_taps[k];
+            for (int k = 0; k < W; ++k) {
+              float row_taps[W];
+              load_taps<W, L::WROW, L::WSW>(wt, tl + k, woff + gl * W, row_taps);
+              wk[k] = row_taps[k];
+            }
           }
           float gv[W][8];
 #pragma unroll

@@ -7,16 +7,19 @@ the C ABI) never touches it, and it shares no code with them.
 The arithmetic lives in ``dsc_oracle.c`` (plain fp64 loops, one function per
 definition; see the comment block at its top for the passages each follows).
 This module marshals torch CPU tensors into it and returns fp64 torch
-tensors; the decode step and the static convolution at the end are
-compositions of those functions (a W-token window through the forward; the
-filter repeated at every token, its gradient summed over tokens in fp64).  Inputs may be float64, float32 or bfloat16; the C side decodes them
-exactly, so the oracle sees the values the GPU sees.
+tensors; the decode step, the decode step merged with its projection and
+the static convolution at the end are compositions of those functions (a
+W-token window through the forward; one fp64 matmul and a rounding before
+that; the filter repeated at every token, its gradient summed over tokens
+in fp64).  Inputs may be float64, float32 or bfloat16; the C side decodes
+them exactly, so the oracle sees the values the GPU sees.
 
 Every function takes an optional ``rows`` (int64 tensor of token indices
 b*T + t); the outputs then hold only those rows, in that order.
 """
 import ctypes
 
+import numpy as np
 import torch
 
 from .build import LIB, build_oracle
@@ -249,6 +252,52 @@ def lowrank_decode(x_t, z_t, U, state, H, W, residual):
     B, C = x_t.shape
     w_t = lowrank_filters(z_t.reshape(B, 1, -1), U, C, H, W).reshape(B, C // H, W)
     return headwise_decode(x_t, w_t, state, H, residual)
+
+
+# ------------------------------------ decode step merged with its projection --
+# "Dynamic Short Convolutions: The 'Locality Bias' Transformers Were
+# Missing", Limitations: for inference the convolution is to be merged into
+# the matmul that precedes it.  In a decode step that matmul is the
+# projection of the new token's hidden state, x_t = h_t Wp^T, with Wp [C, D]
+# stored as a linear layer stores its weight.  The merged step computes what
+# the two separate steps compute: the projection, its result rounded once to
+# the I/O type (the unmerged pair stores x_t in that type), then the decode
+# step above on that x_t.  The projection is one fp64 matmul; the rounding is
+# round-to-nearest-even from the fp64 value.
+
+def round_to(v, dtype):
+    """fp64 tensor rounded to nearest-even `dtype` (torch.bfloat16 or
+    torch.float32), returned in that dtype.  bf16 keeps 8 significant bits:
+    v = m 2^e with 0.5 <= |m| < 1 becomes round_half_even(m 2^8) 2^(e-8)
+    (normal range; the tests' values are far from under- and overflow)."""
+    a = v.detach().double().cpu().numpy()
+    if dtype == torch.float32:
+        return torch.from_numpy(a.astype(np.float32))
+    if dtype != torch.bfloat16:
+        raise ValueError("round_to: bf16 or fp32")
+    m, e = np.frexp(a)
+    q = np.ldexp(np.round(m * 256.0), e - 8)       # np.round: half to even
+    return torch.from_numpy(q).to(torch.bfloat16)   # exact: q is a bf16 value
+
+
+def project(h, Wp, dtype):
+    """x_t [B, C] = h [B, D] Wp[C, D]^T in fp64, rounded to `dtype`."""
+    x64 = h.detach().double().cpu() @ Wp.detach().double().cpu().T
+    return round_to(x64, dtype)
+
+
+def headwise_proj_decode(h, Wp, w_t, state, H, residual):
+    """(y_t, new_state, x_t): the projection, then the head-wise decode step."""
+    x_t = project(h, Wp, h.dtype)
+    y, new_state = headwise_decode(x_t, w_t, state, H, residual)
+    return y, new_state, x_t
+
+
+def lowrank_proj_decode(h, Wp, z_t, U, state, H, W, residual):
+    """(y_t, new_state, x_t): the projection, then the low-rank decode step."""
+    x_t = project(h, Wp, h.dtype)
+    y, new_state = lowrank_decode(x_t, z_t, U, state, H, W, residual)
+    return y, new_state, x_t
 
 
 # -------------------------------------------------- static short conv ------
