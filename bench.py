@@ -566,6 +566,9 @@ def run_dsc(args):
     print(json.dumps(line), flush=True)
     if args.compare_static:
         print(json.dumps(run_compare_static(dev, min(args.steps, 100))), flush=True)
+    if args.compare_decode:
+        print(json.dumps(run_compare_decode(dev, min(args.steps, 100), measured_peaks()[0])),
+              flush=True)
     if args.sweep:
         print(json.dumps(run_sweep(dev, args.sweep_calls)), flush=True)
     return 0
@@ -612,6 +615,66 @@ def run_compare_static(dev, steps):
     return {"comparison": "static_vs_dynamic_short_conv", "unit": "us_per_call",
             "config": {"B": B, "T": T, "C": C, "W": W, "dtype": "bf16", "residual": True},
             "us": out}
+
+
+def run_compare_decode(dev, steps, peak_gbs):
+    """The decode step merged with its projection (one kernel,
+    dsc_headwise_proj_decode) next to the unmerged pair (the projection as a
+    cuBLAS matmul writing x, then dsc_headwise_decode), at the decode shape
+    of the QKV placement: hidden D = 2048, C = 6144 (q, k, v), H = 16, W = 4,
+    bf16, for B = 1, 4, 8, 16 and 64 sequences.  Eight layers' inputs (eight Wp of
+    25 MB: 201 MB, more than L2) are cycled, so each call reads its Wp from
+    HBM as consecutive layers of a model do; the time per call is the event
+    time of `steps` passes over the eight layers divided by the calls."""
+    D, C, H, W, NL = 2048, 6144, 16, 4, 8
+    dt = torch.bfloat16
+    stream = torch.cuda.current_stream()
+    res = {}
+    for B in (1, 4, 8, 16, 64):
+        layers = [syn.proj_decode_inputs(B, D, C, H, W, 0, dt, seed=10 + i, device=dev)
+                  for i in range(NL)]
+        x = torch.empty(B, C, dtype=dt, device=dev)
+        y = torch.empty(B, C, dtype=dt, device=dev)
+        fused = [dsc.bind("dsc_headwise_proj_decode", L["h"], L["Wp"], L["w"], L["state"], y, H,
+                          True) for L in layers]
+        steps_ = [dsc.bind("dsc_headwise_decode", x, L["w"], L["state"], y, H, True)
+                  for L in layers]
+
+        def run_fused():
+            for f in fused:
+                f()
+
+        def run_unmerged():
+            for L, f in zip(layers, steps_):
+                torch.mm(L["h"], L["Wp"].t(), out=x)
+                f()
+
+        out = {}
+        for name, f in (("merged", run_fused), ("unmerged", run_unmerged)):
+            for _ in range(3):
+                f()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(SPIN_CYCLES)
+            a.record(stream)
+            for _ in range(steps):
+                f()
+            b.record(stream)
+            torch.cuda.synchronize()
+            out[name] = a.elapsed_time(b) / (steps * NL) * 1e3
+        nbytes = 2 * (C * D + B * D + B * (C // H) * W + 2 * B * (W - 1) * C + B * C)
+        gbs = nbytes / (out["merged"] * 1e-6) / 1e9
+        res[str(B)] = {"merged_us": round(out["merged"], 2),
+                       "unmerged_us": round(out["unmerged"], 2),
+                       "speedup": round(out["unmerged"] / out["merged"], 3),
+                       "merged_gbs": round(gbs, 1),
+                       "merged_frac_of_hbm_peak": round(gbs / peak_gbs, 4),
+                       "bytes_per_call": nbytes}
+    return {"comparison": "decode_step_merged_with_its_projection_vs_unmerged",
+            "unit": "us_per_call", "kernel_launches_per_call": {"merged": 1, "unmerged": 2},
+            "config": {"D": D, "C": C, "H": H, "W": W, "dtype": "bf16", "residual": True,
+                       "layers_cycled": NL, "l2": "eight layers' weights (201 MB) cycled"},
+            "peak_gbs": peak_gbs, "B": res}
 
 
 def _time_calls(f, n, stream, flush):
@@ -741,6 +804,11 @@ def main():
     ap.add_argument("--sweep-only", action="store_true",
                     help="print only the sweep line (single GPU)")
     ap.add_argument("--sweep-calls", type=int, default=20)
+    ap.add_argument("--compare-decode", action="store_true",
+                    help="also print a line: the decode step merged with its projection "
+                         "vs the unmerged pair")
+    ap.add_argument("--compare-decode-only", action="store_true",
+                    help="print only that line (single GPU)")
     ap.add_argument("--record-traffic", metavar="CSV",
                     help="host only: write profiles/dram_traffic.json from an ncu launch list "
                          "of whole bench steps, then exit")
@@ -754,6 +822,12 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.compare_decode_only:
+        torch.cuda.set_device(0)
+        dsc.load()
+        print(json.dumps(run_compare_decode(torch.device("cuda", 0), min(args.steps, 100),
+                                            measured_peaks()[0])), flush=True)
+        return 0
     if args.compare_static_only:
         torch.cuda.set_device(0)
         dsc.load()

@@ -205,6 +205,44 @@ dsc_status_t dsc_lowrank_decode(const void* x, const void* z, const void* U, voi
                                 int residual, dsc_dtype_t dtype, void* stream);
 
 /*
+ * Decode step merged with the projection that produces its input
+ * ("Dynamic Short Convolutions: The 'Locality Bias' Transformers Were
+ * Missing", Limitations: for inference the convolution is to be merged into
+ * the matmul that precedes it).  The step's input is computed in the same
+ * kernel as
+ *   x[b,c] = sum_{d<D} h[b,d] Wp[c,d]        (fp32 accumulation)
+ * rounded once to the I/O type (the value a separate projection would
+ * store), then the decode step of dsc_headwise_decode runs on it: y and the
+ * state are exactly what that projection followed by dsc_headwise_decode
+ * produce, up to the summation order of x.  x itself is not written; with
+ * W > 1 it is row 0 of the updated state.
+ *   h : [B, D] hidden states of the new tokens    Wp : [C, D] (a linear
+ *   layer's weight: out_features x in_features)   w : [B, C/H, W]
+ *   state : [B, W-1, C], read and updated in place (may be NULL when W = 1)
+ *   y : [B, C]
+ * Same element type for all.  1 <= D <= 2^24 with 16-byte rows (D a
+ * multiple of 8 for bf16, 4 for fp32, else DSC_ERR_ALIGNMENT); B <= 2^24.
+ * y may not alias h or Wp; the state may not alias h, Wp or y.  Other rules
+ * as for dsc_headwise_decode; B = 0 is a no-op.  The kernel streams Wp once
+ * per block of 8 sequences (later blocks from L2), so it is built for
+ * decode batches; it is not a general GEMM.
+ */
+dsc_status_t dsc_headwise_proj_decode(const void* h, const void* Wp, const void* w,
+                                      void* state, void* y, int64_t B, int64_t D,
+                                      int64_t C, int64_t H, int64_t W, int residual,
+                                      dsc_dtype_t dtype, void* stream);
+
+/*
+ * The same for the low-rank parameterisation: the projection as above,
+ * then the step of dsc_lowrank_decode (taps sum_r z[b,r] U[r,g*W+k] in fp32).
+ * z : [B, R], U : [R, (C/H)*W], 1 <= R <= 32.
+ */
+dsc_status_t dsc_lowrank_proj_decode(const void* h, const void* Wp, const void* z,
+                                     const void* U, void* state, void* y, int64_t B,
+                                     int64_t D, int64_t C, int64_t H, int64_t W, int64_t R,
+                                     int residual, dsc_dtype_t dtype, void* stream);
+
+/*
  * Which low-rank kernels these arguments run on: bit 0 set if
  * dsc_lowrank_fwd uses the tensor cores (tcgen05: bf16, R in {8, 16, 24,
  * 32}, 1 <= W <= 4, H = 1, or H > 1 with (64/H)*W and (C/H)*W multiples of

@@ -44,6 +44,15 @@ Shape make_shape(int64_t B, int64_t T, int64_t C, int64_t H, int64_t W, int64_t 
 
 dsc_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSC_OK : DSC_ERR_CUDA; }
 
+// Checks of the projection-merged decode step beyond those of the decode step:
+// D (the hidden size) positive, 16-byte rows, B small enough for the
+// kernel's 32-bit sequence index.
+dsc_status_t check_proj(int64_t B, int64_t D, dsc_dtype_t dtype) {
+  if (D < 1 || D > (int64_t(1) << 24) || B > (int64_t(1) << 24)) return DSC_ERR_INVALID_ARG;
+  if (D % (dtype == DSC_BF16 ? 8 : 4) != 0) return DSC_ERR_ALIGNMENT;
+  return DSC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -171,6 +180,40 @@ dsc_status_t dsc_lowrank_decode(const void* x, const void* z, const void* U, voi
   return from_cuda(dsc::lowrank_decode(x, z, U, state, y,
                                        make_shape(B, 1, C, H, W, R, residual, dtype),
                                        (cudaStream_t)stream));
+}
+
+dsc_status_t dsc_headwise_proj_decode(const void* h, const void* Wp, const void* w, void* state,
+                                      void* y, int64_t B, int64_t D, int64_t C, int64_t H,
+                                      int64_t W, int residual, dsc_dtype_t dtype, void* stream) {
+  dsc_status_t st = check_shape(B, 1, C, H, W, 0, dtype, false);
+  if (st != DSC_OK) return st;
+  if ((st = check_proj(B, D, dtype)) != DSC_OK) return st;
+  if (B == 0) return DSC_OK;
+  if ((st = check_ptrs({h, Wp, w, y})) != DSC_OK) return st;
+  if (W > 1 && (st = check_ptrs({state})) != DSC_OK) return st;
+  if (y == h || y == Wp || (W > 1 && (state == h || state == y || state == Wp)))
+    return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::headwise_proj_decode(h, Wp, w, state, y,
+                                             make_shape(B, 1, C, H, W, 0, residual, dtype), D,
+                                             (cudaStream_t)stream));
+}
+
+dsc_status_t dsc_lowrank_proj_decode(const void* h, const void* Wp, const void* z, const void* U,
+                                     void* state, void* y, int64_t B, int64_t D, int64_t C,
+                                     int64_t H, int64_t W, int64_t R, int residual,
+                                     dsc_dtype_t dtype, void* stream) {
+  dsc_status_t st = check_shape(B, 1, C, H, W, R, dtype, true);
+  if (st != DSC_OK) return st;
+  if ((st = check_proj(B, D, dtype)) != DSC_OK) return st;
+  if (R > 32) return DSC_ERR_UNSUPPORTED;
+  if (B == 0) return DSC_OK;
+  if ((st = check_ptrs({h, Wp, z, U, y})) != DSC_OK) return st;
+  if (W > 1 && (st = check_ptrs({state})) != DSC_OK) return st;
+  if (y == h || y == Wp || (W > 1 && (state == h || state == y || state == Wp)))
+    return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::lowrank_proj_decode(h, Wp, z, U, state, y,
+                                            make_shape(B, 1, C, H, W, R, residual, dtype), D,
+                                            (cudaStream_t)stream));
 }
 
 dsc_status_t dsc_static_fwd(const void* x, const void* w, void* y, int64_t B, int64_t T,

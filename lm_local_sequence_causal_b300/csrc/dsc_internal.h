@@ -41,6 +41,15 @@ cudaError_t headwise_decode(const void* x, const void* w, void* state, void* y, 
 cudaError_t lowrank_decode(const void* x, const void* z, const void* U, void* state, void* y,
                            const Shape& s, cudaStream_t st);
 
+// Decode step merged with the projection of its input, x_t = h Wp^T with
+// h [B, D] and Wp [C, D] (proj_decode.cu); s.T is 1, D a multiple of the
+// 16-byte vector width.
+cudaError_t headwise_proj_decode(const void* h, const void* Wp, const void* w, void* state,
+                                 void* y, const Shape& s, int64_t D, cudaStream_t st);
+cudaError_t lowrank_proj_decode(const void* h, const void* Wp, const void* z, const void* U,
+                                void* state, void* y, const Shape& s, int64_t D,
+                                cudaStream_t st);
+
 // Static short convolution, filters w [C, W] constant over t (static_conv.cu).
 // H = 1.  The backward needs a caller-owned fp32 workspace for the dw partials.
 cudaError_t static_fwd(const void* x, const void* w, void* y, const Shape& s, cudaStream_t st);

@@ -68,6 +68,12 @@ def load():
     lib.dsc_static_bwd.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64, INT, INT, P]
     lib.dsc_static_bwd.restype = INT
     lib.dsc_lowrank_decode.restype = INT
+    lib.dsc_headwise_proj_decode.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, INT,
+                                             INT, P]
+    lib.dsc_headwise_proj_decode.restype = INT
+    lib.dsc_lowrank_proj_decode.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, I64,
+                                            INT, INT, P]
+    lib.dsc_lowrank_proj_decode.restype = INT
     lib.dsc_lowrank_uses_tensor_cores.argtypes = [I64, I64, I64, I64, I64, I64, INT]
     lib.dsc_lowrank_uses_tensor_cores.restype = INT
     lib.dsc_headwise_uses_tma.argtypes = [I64, I64, I64, I64, I64, INT]
@@ -224,6 +230,31 @@ def _m_dsc_lowrank_decode(x, z, U, state, y, H, W, residual=True, stream=None):
             B, C, H, W, R, int(bool(residual)), _dtype_code(x), _stream(stream))
 
 
+def _m_dsc_headwise_proj_decode(h, Wp, w, state, y, H, residual=True, stream=None):
+    if h.dim() != 2 or Wp.dim() != 2:
+        raise ValueError("h must be [B, D] and Wp [C, D]")
+    B, D = h.shape
+    C = Wp.shape[0]
+    W = w.shape[-1]
+    dt = h.dtype
+    sp = _ptr(state, dt, "state") if W > 1 else None
+    return (_ptr(h, dt, "h"), _ptr(Wp, dt, "Wp"), _ptr(w, dt, "w"), sp, _ptr(y, dt, "y"),
+            B, D, C, H, W, int(bool(residual)), _dtype_code(h), _stream(stream))
+
+
+def _m_dsc_lowrank_proj_decode(h, Wp, z, U, state, y, H, W, residual=True, stream=None):
+    if h.dim() != 2 or Wp.dim() != 2:
+        raise ValueError("h must be [B, D] and Wp [C, D]")
+    B, D = h.shape
+    C = Wp.shape[0]
+    R = z.shape[-1]
+    dt = h.dtype
+    sp = _ptr(state, dt, "state") if W > 1 else None
+    return (_ptr(h, dt, "h"), _ptr(Wp, dt, "Wp"), _ptr(z, dt, "z"), _ptr(U, dt, "U"), sp,
+            _ptr(y, dt, "y"), B, D, C, H, W, R, int(bool(residual)), _dtype_code(h),
+            _stream(stream))
+
+
 def _m_dsc_static_fwd(x, w, y, residual=True, stream=None):
     B, T, C = _bt_c(x)
     W = w.shape[-1]
@@ -288,6 +319,19 @@ def dsc_lowrank_decode(x, z, U, state, y, H, W, residual=True, stream=None):
     """Low-rank decode step: taps z [B,R] U formed in fp32, then as above."""
     _call("dsc_lowrank_decode",
           _m_dsc_lowrank_decode(x, z, U, state, y, H, W, residual, stream))
+
+
+def dsc_headwise_proj_decode(h, Wp, w, state, y, H, residual=True, stream=None):
+    """Decode step merged with its projection: x = h [B,D] Wp[C,D]^T rounded
+    once to the I/O type inside the kernel, then the head-wise decode step."""
+    _call("dsc_headwise_proj_decode",
+          _m_dsc_headwise_proj_decode(h, Wp, w, state, y, H, residual, stream))
+
+
+def dsc_lowrank_proj_decode(h, Wp, z, U, state, y, H, W, residual=True, stream=None):
+    """The same with the low-rank decode step (taps z [B,R] U in fp32)."""
+    _call("dsc_lowrank_proj_decode",
+          _m_dsc_lowrank_proj_decode(h, Wp, z, U, state, y, H, W, residual, stream))
 
 
 def dsc_static_fwd(x, w, y, residual=True, stream=None):

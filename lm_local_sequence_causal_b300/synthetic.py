@@ -5,7 +5,8 @@ draws random tensors and nothing else.  It holds none of the method's
 arithmetic (no convolution, no filter generation, no gradient).
 
 Each tensor is drawn from a torch generator seeded with ``seed * 16 + slot``
-(slot 0 = x, 1 = w, 2 = dy, 3 = z, 4 = U, 5 = the hot-channel permutation), as
+(slot 0 = x, 1 = w, 2 = dy, 3 = z, 4 = U, 5 = the hot-channel permutation,
+6 = h, 7 = Wp, 8 = a decode state), as
 fp32 N(0, 1) scaled by its standard deviation, then rounded once to the I/O
 dtype.  Both sides consume the rounded tensor, so they see identical values.
 Draws on a CUDA device use torch's CUDA generator (fast for the full-size
@@ -25,13 +26,19 @@ deviation a):
   linear_rnn      B=2 T=16384 C=4096 W=4; head-wise H=64, low-rank R=16;
                   x ~ N(0,1) with round(0.05 C) channels (a seeded random
                   choice) scaled by 8 to stress accumulation.
+  decode with its projection (``proj_decode_inputs``): hidden states
+                  h [B,D] ~ N(0,1) (slot 6), projection weight Wp [C,D] std
+                  1/sqrt(D) (slot 7, so x = h Wp^T is about N(0,1)), state
+                  [B,W-1,C] ~ N(0,1) (slot 8), and w [B,G,W] std 0.5 or z
+                  [B,R], U [R,G*W] std 1/sqrt(R) for the filters; the decode
+                  shape of the QKV placement is B=8, D=2048, C=6144, H=16, W=4.
 """
 from dataclasses import dataclass, replace
 import math
 
 import torch
 
-SLOT_X, SLOT_W, SLOT_DY, SLOT_Z, SLOT_U, SLOT_HOT = range(6)
+SLOT_X, SLOT_W, SLOT_DY, SLOT_Z, SLOT_U, SLOT_HOT, SLOT_H, SLOT_WP, SLOT_STATE = range(9)
 
 
 @dataclass(frozen=True)
@@ -146,6 +153,22 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu", need_grad_inputs=True
         out["w"] = draw((B, T, wl.G, W), wl.w_std, seed, SLOT_W, wl.dtype, device)
     if need_grad_inputs:
         out["dy"] = draw((B, T, C), 1.0, seed, SLOT_DY, wl.dtype, device)
+    return out
+
+
+def proj_decode_inputs(B, D, C, H, W, R=0, dtype=torch.bfloat16, seed=0, device="cpu"):
+    """Inputs of one decode step merged with its projection: h [B,D],
+    Wp [C,D], state [B,W-1,C], and w [B,C/H,W] (R = 0) or z [B,R], U [R,(C/H)*W]."""
+    out = {
+        "h": draw((B, D), 1.0, seed, SLOT_H, dtype, device),
+        "Wp": draw((C, D), 1.0 / math.sqrt(D), seed, SLOT_WP, dtype, device),
+        "state": draw((B, max(W - 1, 0), C), 1.0, seed, SLOT_STATE, dtype, device),
+    }
+    if R:
+        out["z"] = draw((B, R), 1.0 / math.sqrt(R), seed, SLOT_Z, dtype, device)
+        out["U"] = draw((R, (C // H) * W), 1.0 / math.sqrt(R), seed, SLOT_U, dtype, device)
+    else:
+        out["w"] = draw((B, C // H, W), 0.5, seed, SLOT_W, dtype, device)
     return out
 
 

@@ -190,3 +190,29 @@ def test_selftest_entry_points_validate_on_the_host(lib):
              BF16, ok_limit, None) == dsc.DSC_ERR_WORKSPACE
     assert g(A, A2, A3, A4, A5, P(0x60000), P(0x70000), P(0x80000), 1 << 30, 2, 256, 128, 1, 4,
              16, 1, BF16, u64(10), None) == dsc.DSC_ERR_INVALID_ARG
+
+
+def test_proj_decode_validation(lib):
+    # (h, Wp, w, state, y, B, D, C, H, W, residual, dtype)
+    f = lib.dsc_headwise_proj_decode
+    assert f(A, A2, A3, A4, A5, 8, 2044, 6144, 16, 4, 1, BF16, None) == dsc.DSC_ERR_ALIGNMENT
+    assert f(A, A2, A3, A4, A5, 8, 2046, 6144, 16, 4, 1, F32, None) == dsc.DSC_ERR_ALIGNMENT
+    assert f(A, A2, A3, A4, A5, 8, 0, 6144, 16, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, A4, A5, 8, 2048, 6144, 16, 5, 1, BF16, None) == dsc.DSC_ERR_UNSUPPORTED
+    assert f(A, A2, A3, A4, A5, 8, 2048, 6008, 16, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, A4, A, 8, 2048, 6144, 16, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, A5, A5, 8, 2048, 6144, 16, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, A2, A5, 8, 2048, 6144, 16, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, None, A5, 8, 2048, 6144, 16, 4, 1, BF16, None) == dsc.DSC_ERR_INVALID_ARG
+    assert f(MIS, A2, A3, A4, A5, 8, 2048, 6144, 16, 4, 1, BF16, None) == dsc.DSC_ERR_ALIGNMENT
+    assert f(None, None, None, None, None, 0, 2048, 6144, 16, 4, 1, BF16, None) == dsc.DSC_OK
+    g = lib.dsc_lowrank_proj_decode
+    # (h, Wp, z, U, state, y, B, D, C, H, W, R, residual, dtype)
+    assert g(A, A2, A3, A4, A5, P(0x60000), 8, 2048, 6144, 1, 4, 33, 1, BF16,
+             None) == dsc.DSC_ERR_UNSUPPORTED
+    assert g(A, A2, A3, A4, A5, P(0x60000), 8, 2048, 6144, 1, 4, 0, 1, BF16,
+             None) == dsc.DSC_ERR_INVALID_ARG
+    assert g(A, A2, A3, None, A5, P(0x60000), 8, 2048, 6144, 1, 4, 16, 1, BF16,
+             None) == dsc.DSC_ERR_INVALID_ARG
+    assert g(A, A2, A3, A4, A5, P(0x60000), 8, 12, 6144, 1, 4, 16, 1, BF16,
+             None) == dsc.DSC_ERR_ALIGNMENT
