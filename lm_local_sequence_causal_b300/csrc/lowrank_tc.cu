@@ -120,16 +120,18 @@ struct FwdLayout {
 
 // Work item i of the forward -> (b, token tile, chunk): tile-major, so the
 // CTAs working side by side (items i, i+1, ... handed out round-robin) read
-// neighbouring 128-byte pieces of the same rows of x.
+// neighbouring 128-byte pieces of the same rows of x.  32-bit arithmetic:
+// the host admits fewer than 2^31 items (lowrank_tc_supported).
 struct Item {
   int chunk, b, t0;
 };
 __device__ __forceinline__ Item decode_tm(long long i, int nchunks, int ntiles) {
   Item it;
-  const long long tile = i / nchunks;
-  it.chunk = static_cast<int>(i - tile * nchunks);
-  it.b = static_cast<int>(tile / ntiles);
-  it.t0 = static_cast<int>(tile - static_cast<long long>(it.b) * ntiles) * BM;
+  const unsigned ii = static_cast<unsigned>(i);
+  const unsigned tile = ii / static_cast<unsigned>(nchunks);
+  it.chunk = static_cast<int>(ii - tile * static_cast<unsigned>(nchunks));
+  it.b = static_cast<int>(tile / static_cast<unsigned>(ntiles));
+  it.t0 = static_cast<int>(tile - static_cast<unsigned>(it.b) * static_cast<unsigned>(ntiles)) * BM;
   return it;
 }
 
@@ -171,12 +173,14 @@ __host__ __device__ constexpr uint32_t idesc_major(uint32_t M, uint32_t N, uint3
   return idesc_bf16_f32(M, N) | (amaj << 15) | (bmaj << 16);
 }
 
-template <int W, int KS, int HP>
+// RES: y includes the residual x (a template parameter: as a runtime flag
+// its select sat in every piece of the epilogue, measured 2% slower).
+template <int W, int KS, int HP, bool RES>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
           const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_y,
-          int ntiles, int nbt, int nchunks, int residual, int hshift, uint64_t wns,
-          int withhold, int C, int T) {
+          int ntiles, int nbt, int nchunks, int hshift, uint64_t wns, int withhold, int C,
+          int T) {
   using L = FwdLayout<W, KS, HP>;
   const int ucols = (CC >> hshift) * W;      // U columns of one chunk (H = 2^hshift)
   extern __shared__ unsigned char smem_raw[];
@@ -326,7 +330,7 @@ lr_fwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         float2 o[4];
         const uint32_t x0[4] = {xr[0].x, xr[0].y, xr[0].z, xr[0].w};
 #pragma unroll
-        for (int p = 0; p < 4; ++p) o[p] = residual ? bf2f(x0[p]) : make_float2(0.f, 0.f);
+        for (int p = 0; p < 4; ++p) o[p] = RES ? bf2f(x0[p]) : make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < W; ++k) {
           const uint32_t xw[4] = {xr[k].x, xr[k].y, xr[k].z, xr[k].w};
@@ -1054,7 +1058,12 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, si
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int W, int KS, int HP>
+// The shared-memory opt-in is recorded per kernel instance; the two RES
+// instances of a layout are two kernels.
+template <int W, int KS, int HP, bool RES>
+struct FwdKernelTag {};
+
+template <int W, int KS, int HP, bool RES>
 cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, const Shape& s,
                        cudaStream_t st, const Diag& dg) {
   using L = FwdLayout<W, KS, HP>;
@@ -1071,11 +1080,11 @@ cudaError_t launch_fwd(const void* x, const void* z, const void* U, void* y, con
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   const long long grid = std::min<long long>(sms, items);
-  auto kern = lr_fwd_tc<W, KS, HP>;
-  cudaError_t e = set_smem<L>(kern, L::TOTAL);
+  auto kern = lr_fwd_tc<W, KS, HP, RES>;
+  cudaError_t e = set_smem<FwdKernelTag<W, KS, HP, RES>>(kern, L::TOTAL);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(grid), kFwdThreads, L::TOTAL, st>>>(
-      tx, tz, tu, ty, ntiles, static_cast<int>(nbt), nchunks, s.residual,
+      tx, tz, tu, ty, ntiles, static_cast<int>(nbt), nchunks,
       __builtin_ctzll(static_cast<unsigned long long>(s.H)), dg.wait_ns, dg.withhold,
       static_cast<int>(s.C), static_cast<int>(s.T));
   return cudaGetLastError();
@@ -1210,15 +1219,22 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
   return cudaGetLastError();
 }
 
+template <int KS, int HP, bool RES>
+cudaError_t fwd_res(const void* x, const void* z, const void* U, void* y, const Shape& s,
+                    cudaStream_t st, const Diag& dg) {
+  switch (s.W) {
+    case 1: return launch_fwd<1, KS, HP, RES>(x, z, U, y, s, st, dg);
+    case 2: return launch_fwd<2, KS, HP, RES>(x, z, U, y, s, st, dg);
+    case 3: return launch_fwd<3, KS, HP, RES>(x, z, U, y, s, st, dg);
+    default: return launch_fwd<4, KS, HP, RES>(x, z, U, y, s, st, dg);
+  }
+}
+
 template <int KS, int HP>
 cudaError_t fwd_hp(const void* x, const void* z, const void* U, void* y, const Shape& s,
                    cudaStream_t st, const Diag& dg) {
-  switch (s.W) {
-    case 1: return launch_fwd<1, KS, HP>(x, z, U, y, s, st, dg);
-    case 2: return launch_fwd<2, KS, HP>(x, z, U, y, s, st, dg);
-    case 3: return launch_fwd<3, KS, HP>(x, z, U, y, s, st, dg);
-    default: return launch_fwd<4, KS, HP>(x, z, U, y, s, st, dg);
-  }
+  return s.residual ? fwd_res<KS, HP, true>(x, z, U, y, s, st, dg)
+                    : fwd_res<KS, HP, false>(x, z, U, y, s, st, dg);
 }
 
 template <int KS>
@@ -1294,7 +1310,8 @@ bool lowrank_tc_supported(const Shape& s) {
                                    (s.G() * s.W) % 8 == 0);
   return s.bf16 && tie_ok && s.R >= 8 && s.R <= 32 && s.R % 8 == 0 && s.W >= 1 && s.W <= 4 &&
          s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.T < (int64_t(1) << 30) &&
-         s.C < (int64_t(1) << 24);
+         s.C < (int64_t(1) << 24) &&
+         s.B * ((s.T + BM - 1) / BM) * ((s.C + CC - 1) / CC) < (int64_t(1) << 31);
 }
 
 namespace {
