@@ -62,11 +62,12 @@ def test_batch_blocks(B):
     _run(torch.bfloat16, B=B, D=512, C=256, H=16, W=4, seed=B)
 
 
-@pytest.mark.parametrize("D", [8, 24, 256, 264, 1000, 4096])
-def test_hidden_sizes(D):
+@pytest.mark.parametrize("D", [8, 24, 256, 264, 1000, 3072, 3080, 4096, 6144, 6152])
+@pytest.mark.parametrize("B", [3, 9])
+def test_hidden_sizes(D, B):
     # one piece per row, fewer pieces than lanes, pieces not a multiple of the
-    # lanes x pieces in flight, and a long row
-    _run(torch.bfloat16, B=3, D=D, C=128, H=8, W=3, seed=D)
+    # lanes x pieces in flight, and long rows; both kernels (B = 3 and 9)
+    _run(torch.bfloat16, B=B, D=D, C=128, H=8, W=3, seed=D + B)
 
 
 @pytest.mark.parametrize("residual", [False, True])
@@ -77,7 +78,7 @@ def test_residual_switch(residual):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("W", [2, 4])
 @pytest.mark.parametrize("R,H", [(16, 1), (3, 1), (16, 4), (32, 1)])
-@pytest.mark.parametrize("B", [3, 20])
+@pytest.mark.parametrize("B", [3, 20, 40])
 def test_lowrank_step(dtype, W, R, H, B):
     _run(dtype, B=B, D=256, C=512, H=H, W=W, R=R, seed=R + W + B)
 
