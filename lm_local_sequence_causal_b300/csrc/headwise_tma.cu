@@ -167,15 +167,15 @@ __device__ __forceinline__ void load_taps(uint32_t wt, uint32_t r, int e0, float
 struct HwItem {
   int chunk, b, t0;
 };
-// Work item i -> (chunk, b, t0), tile-major; 32-bit arithmetic (the host
-// admits fewer than 2^31 items, headwise_tma_supported).
+// Work item i -> (chunk, b, t0), tile-major.  (The same in 32-bit
+// arithmetic measured 5% slower in the forward at the QKV size: 82.0 against
+// 77.9 us; the compiler scheduled the epilogue differently.)
 __device__ __forceinline__ HwItem hw_decode(long long i, int nchunks, int ntiles) {
   HwItem it;
-  const unsigned ii = static_cast<unsigned>(i);
-  const unsigned tile = ii / static_cast<unsigned>(nchunks);
-  it.chunk = static_cast<int>(ii - tile * static_cast<unsigned>(nchunks));
-  it.b = static_cast<int>(tile / static_cast<unsigned>(ntiles));
-  it.t0 = static_cast<int>(tile - static_cast<unsigned>(it.b) * static_cast<unsigned>(ntiles)) * BM;
+  const long long tile = i / nchunks;
+  it.chunk = static_cast<int>(i - tile * nchunks);
+  it.b = static_cast<int>(tile / ntiles);
+  it.t0 = static_cast<int>(tile - static_cast<long long>(it.b) * ntiles) * BM;
   return it;
 }
 
@@ -587,8 +587,7 @@ bool headwise_tma_supported(const Shape& s, bool bwd) {
   if (!s.bf16) return false;
   const int cw = item_width(s.H, s.W, bwd, s.C);
   return cw > 0 && s.T < (int64_t(1) << 30) &&
-         s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.C < (int64_t(1) << 24) &&
-         s.B * ((s.T + BM - 1) / BM) * (s.C / cw) < (int64_t(1) << 31);
+         s.B * ((s.T + BM - 1) / BM) < (int64_t(1) << 30) && s.C < (int64_t(1) << 24);
 }
 
 cudaError_t headwise_fwd_tma(const void* x, const void* w, void* y, const Shape& s,
