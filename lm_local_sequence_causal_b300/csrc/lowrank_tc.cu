@@ -444,7 +444,7 @@ struct BwdArgs {
   float* dz_part;          // [S][B*T][RP]
   float* dU_part;          // [P][RP][C*W]
   const unsigned char* uimg;  // [nchunks][W][RP rows][128 B] swizzled U tiles
-  int T, C, ntiles, nchunks, S, P, ntl, residual;
+  int T, C, ntiles, nchunks, S, P, ntl;
   // Bounded waits give up after wait_ns; withhold != 0 makes the producer
   // issue no loads at all, so every wait of the other roles runs out (the
   // self-test of the failure path; 0 in normal use).
@@ -452,7 +452,10 @@ struct BwdArgs {
   int withhold;
 };
 
-template <int W, int RK>
+// RES: dx includes the residual dy (a template parameter: as the runtime
+// flag it was a select per 8-channel piece on the dx warps' path, measured
+// 2% slower).
+template <int W, int RK, bool RES>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
           const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dx,
@@ -730,11 +733,24 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       const int wd = warp - 2;                              // 0..7 within the group
       const uint32_t dxst = sb + L::DX_OFF + wd * kDParts * L::DXBOX;
       const uint64_t pol_dx = policy_evict_first();
-      for (int n = 0; n < nitems; ++n) {
-        const int lc = n / ntile, lt = n - lc * ntile;
+      // Item n = chunk lc, tile lt of the split = tile tt of sequence b,
+      // advanced item by item (no division on this path).
+      const int b_first = tl0 / args.ntiles, tt_first = tl0 - b_first * args.ntiles;
+      int lc = 0, lt = 0, b = b_first, tt = tt_first;
+      auto next_item = [&]() {
+        if (++lt == ntile) {
+          lt = 0;
+          ++lc;
+          b = b_first;
+          tt = tt_first;
+        } else if (++tt == args.ntiles) {
+          tt = 0;
+          ++b;
+        }
+      };
+      for (int n = 0; n < nitems; ++n, next_item()) {
         const int s = n % NST_;
-        const int gt = tl0 + lt;
-        const int b = gt / args.ntiles, t0 = (gt - b * args.ntiles) * BM;
+        const int t0 = tt * BM;
         const int c0 = (ch0 + lc) * CC;
         const uint32_t dyt = sb + L::STG_OFF + s * L::STAGE + L::XBYTES;
         ok = mbar_wait(bar_full + 8 * s, (n / NST_) & 1, abort_flag, &g_tc_error, 3, wns);
@@ -780,7 +796,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
               if (k == 0) {
 #pragma unroll
                 for (int p = 0; p < 4; ++p)
-                  o[p] = args.residual ? bf2f(gw[p]) : make_float2(0.f, 0.f);
+                  o[p] = RES ? bf2f(gw[p]) : make_float2(0.f, 0.f);
               }
 #pragma unroll
               for (int p = 0; p < 4; ++p)
@@ -813,8 +829,14 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       const int wt = threadIdx.x - (2 + NEPI) * 32;     // 0..255 in the dw group
       const int wc = wt & 7;                            // 16-byte chunk of the row
       const int r0 = (wt >> 3) * 4;                     // first token of the run
-      for (int n = 0; n < nitems; ++n) {
-        const int lc = n / ntile, lt = n - lc * ntile;
+      int lc = 0, lt = 0;                               // chunk and tile of item n
+      auto next_item = [&]() {
+        if (++lt == ntile) {
+          lt = 0;
+          ++lc;
+        }
+      };
+      for (int n = 0; n < nitems; ++n, next_item()) {
         const int s = n % NST_;
         const int c0 = (ch0 + lc) * CC;
         const uint32_t xt = sb + L::STG_OFF + s * L::STAGE, dyt = xt + L::XBYTES;
@@ -1154,7 +1176,12 @@ TcBwdPlan plan_bwd_tc(const Shape& s, int nsm) {
   return p;
 }
 
-template <int W, int RK>
+// One shared-memory opt-in record per backward kernel instance (the RES
+// instances of a layout are two kernels).
+template <int W, int RK, bool RES>
+struct BwdKernelTag {};
+
+template <int W, int RK, bool RES>
 cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* dy, void* dx,
                        void* dz, void* dU, void* ws, const Shape& s, const TcBwdPlan& p,
                        cudaStream_t st, const Diag& dg) {
@@ -1184,7 +1211,6 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
   a.S = p.S;
   a.P = p.P;
   a.ntl = p.ntl;
-  a.residual = s.residual;
   a.wait_ns = dg.wait_ns;
   a.withhold = dg.withhold;
   {
@@ -1196,8 +1222,8 @@ cudaError_t launch_bwd(const void* x, const void* z, const void* U, const void* 
     if (e != cudaSuccess) return e;
   }
   static_assert(L::TOTAL <= 227 * 1024, "backward shared memory");
-  auto kern = lr_bwd_tc<W, RK>;
-  cudaError_t e = set_smem<L>(kern, L::TOTAL);
+  auto kern = lr_bwd_tc<W, RK, RES>;
+  cudaError_t e = set_smem<BwdKernelTag<W, RK, RES>>(kern, L::TOTAL);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, static_cast<unsigned>(p.S * p.P), kBwdThreads, L::TOTAL, st, tx, tdy, tz,
                  tdx, a);
@@ -1248,6 +1274,14 @@ cudaError_t fwd_w(const void* x, const void* z, const void* U, void* y, const Sh
   }
 }
 
+template <int W, int RK>
+cudaError_t bwd_res(const void* x, const void* z, const void* U, const void* dy, void* dx,
+                    void* dz, void* dU, void* ws, const Shape& s, const TcBwdPlan& p,
+                    cudaStream_t st, const Diag& dg) {
+  return s.residual ? launch_bwd<W, RK, true>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg)
+                    : launch_bwd<W, RK, false>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+}
+
 cudaError_t bwd_dispatch(const void* x, const void* z, const void* U, const void* dy, void* dx,
                          void* dz, void* dU, void* ws, const Shape& s, cudaStream_t st,
                          const Diag& dg) {
@@ -1256,17 +1290,17 @@ cudaError_t bwd_dispatch(const void* x, const void* z, const void* U, const void
   const TcBwdPlan p = plan_bwd_tc(s, nsm);
   if (rk_of(s.R) == 2) {
     switch (s.W) {
-      case 1: return launch_bwd<1, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
-      case 2: return launch_bwd<2, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
-      case 3: return launch_bwd<3, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
-      default: return launch_bwd<4, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+      case 1: return bwd_res<1, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+      case 2: return bwd_res<2, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+      case 3: return bwd_res<3, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+      default: return bwd_res<4, 2>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
     }
   }
   switch (s.W) {
-    case 1: return launch_bwd<1, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
-    case 2: return launch_bwd<2, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
-    case 3: return launch_bwd<3, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
-    default: return launch_bwd<4, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+    case 1: return bwd_res<1, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+    case 2: return bwd_res<2, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+    case 3: return bwd_res<3, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
+    default: return bwd_res<4, 1>(x, z, U, dy, dx, dz, dU, ws, s, p, st, dg);
   }
 }
 
