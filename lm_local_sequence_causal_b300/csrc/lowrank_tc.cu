@@ -537,15 +537,29 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
   griddep_wait();
   griddep_launch_dependents();
 
-  // item n -> (local chunk lc = n / ntile, local tile lt = n % ntile)
+  // item n -> (local chunk lc = n / ntile, local tile lt = n % ntile), tracked
+  // item by item in every role
   if (warp == 0) {
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();
+      // item n = chunk lc, tile lt of the split = tile tt of sequence b
+      const int b_first = tl0 / args.ntiles, tt_first = tl0 - b_first * args.ntiles;
+      int lc = 0, lt = 0, b = b_first, tt = tt_first;
+      auto next_item = [&]() {
+        if (++lt == ntile) {
+          lt = 0;
+          ++lc;
+          b = b_first;
+          tt = tt_first;
+        } else if (++tt == args.ntiles) {
+          tt = 0;
+          ++b;
+        }
+      };
       int n = 0;
-      for (; n < nitems && !args.withhold; ++n) {
-        const int lc = n / ntile, lt = n - lc * ntile;
+      for (; n < nitems && !args.withhold; ++n, next_item()) {
         if (lt == 0) {
           const int ub = lc & 1;
           if (!mbar_wait(bar_ufree + 8 * ub, ((lc >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 1,
@@ -563,8 +577,7 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int s = n % NST_;
         const uint32_t ph = (n / NST_) & 1;
         if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_tc_error, 1, wns)) break;
-        const int gt = tl0 + lt;
-        const int b = gt / args.ntiles, t0 = (gt - b * args.ntiles) * BM;
+        const int t0 = tt * BM;
         const int c0 = (ch0 + lc) * CC;
         const uint32_t full = bar_full + 8 * s;
         const uint32_t st = sb + L::STG_OFF + s * L::STAGE;
@@ -595,8 +608,14 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       const uint32_t zsbo = L::XROWS * 16;                    // stride of the two z halves
       int issued[kDParts] = {};
       bool ok = true;
-      for (int n = 0; n < nitems && ok; ++n) {
-        const int lc = n / ntile, lt = n - lc * ntile;
+      int lc = 0, lt = 0;                          // chunk and tile of item n
+      auto next_item = [&]() {
+        if (++lt == ntile) {
+          lt = 0;
+          ++lc;
+        }
+      };
+      for (int n = 0; n < nitems && ok; ++n, next_item()) {
         const int s = n % NST_;
         if (lt == 0)
           ok = mbar_wait(bar_ufull + 8 * (lc & 1), (lc >> 1) & 1, abort_flag, &g_tc_error, 2,
@@ -650,8 +669,14 @@ lr_bwd_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
       const uint32_t zsbo = L::XROWS * 16;
       bool ok = true;
       int issued_pair[2] = {0, 0};
-      for (int m = 0; m < nitems && ok; ++m) {
-        const int lc = m / ntile, lt = m - lc * ntile;
+      int lc = 0, lt = 0;                          // chunk and tile of item m
+      auto next_item = [&]() {
+        if (++lt == ntile) {
+          lt = 0;
+          ++lc;
+        }
+      };
+      for (int m = 0; m < nitems && ok; ++m, next_item()) {
         const int s = m % NST_;
         const int ub = lc & 1;
         if (lt == 0) {
