@@ -274,7 +274,40 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     const uint64_t pol = policy_evict_first();
     const uint32_t obuf = sb + L::O_OFF + g * L::OBYTES;
     const uint32_t dwbuf = sb + L::DW_OFF + g * L::DWBYTES;
-    for (int it = g; it < nmine; it += 2) {
+    // TRACK: the group's items (g, g+2, ... of this CTA) are followed step by
+    // step: the global item moves by 2 * gridDim.x, i.e. dch chunks and dtl
+    // (b, tile) steps with carries.  Used by the backward with H >= 16, where
+    // it measured faster than decoding each item with divisions (QKV pair
+    // 119.6 -> 117.6 us, H = 64 147.5 -> 144.3 us); the forward and H = 8
+    // measured slower with it (78 -> 82 us, 130 -> 137 us: the compiler
+    // scheduled their epilogues differently) and decode each item.
+    constexpr bool TRACK = BWD && H >= 16;
+    HwItem trk{};
+    int ctl = 0, dtl = 0, dch = 0;
+    if constexpr (TRACK) {
+      trk = hw_decode(blockIdx.x + static_cast<long long>(g) * gridDim.x, nchunks, ntiles);
+      const int istep = 2 * static_cast<int>(gridDim.x);
+      dtl = istep / nchunks;
+      dch = istep - dtl * nchunks;
+      ctl = trk.t0 / BM;
+    }
+    auto next_item = [&]() {
+      if constexpr (TRACK) {
+        trk.chunk += dch;
+        int adv = dtl;
+        if (trk.chunk >= nchunks) {
+          trk.chunk -= nchunks;
+          ++adv;
+        }
+        ctl += adv;
+        while (ctl >= ntiles) {
+          ctl -= ntiles;
+          ++trk.b;
+        }
+        trk.t0 = ctl * BM;
+      }
+    };
+    for (int it = g; it < nmine; it += 2, next_item()) {
       const int s = it % NST;
       const uint32_t aph = (it >> 1) & 1;
       if (storer) {
@@ -288,7 +321,8 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
       const uint32_t wt = st + L::W_IN;
       // PADW: the item's taps start woff elements into the w box.
       const HwItem itm0 =
-          hw_decode(blockIdx.x + static_cast<long long>(it) * gridDim.x, nchunks, ntiles);
+          TRACK ? trk
+                : hw_decode(blockIdx.x + static_cast<long long>(it) * gridDim.x, nchunks, ntiles);
       const int woff = L::PADW ? (itm0.chunk * L::GI * W) & 7 : 0;
       if constexpr (!BWD) {
         // y = res*x + sum_k w[t,g,k] x[t-k].  A group's taps are loaded at
@@ -437,7 +471,8 @@ hw_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
       }
       if (storer && mbar_wait(bar_ofull + 8 * g, aph, abort_flag, &g_hw_error, 4)) {
         const HwItem itm =
-            hw_decode(blockIdx.x + static_cast<long long>(it) * gridDim.x, nchunks, ntiles);
+            TRACK ? trk
+                  : hw_decode(blockIdx.x + static_cast<long long>(it) * gridDim.x, nchunks, ntiles);
 #pragma unroll
         for (int j = 0; j < NB; ++j)
           tma_store_3d(&tm_out, obuf + j * L::OBOX, itm.chunk * CW + 64 * j, itm.t0, itm.b, pol);

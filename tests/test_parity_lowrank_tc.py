@@ -46,9 +46,12 @@ def test_fwd_every_width_every_rank(W, R):
 
 
 @pytest.mark.parametrize("residual", [False, True])
-def test_fwd_residual_flag(residual):
-    wl = syn.Workload("tc_fwd_res", B=3, T=257, C=192, W=4, H=1, R=16, residual=residual)
-    y, ry = run_fwd(wl, seed=3)
+@pytest.mark.parametrize("W,R", [(4, 16), (1, 16), (3, 16), (4, 32)])
+def test_fwd_residual_flag(residual, W, R):
+    # the residual flag is compiled into the forward too
+    wl = syn.Workload("tc_fwd_res", B=3, T=257, C=192, W=W, H=1, R=R, residual=residual,
+                      zu_std=R ** -0.5)
+    y, ry = run_fwd(wl, seed=3 + W + R)
     assert_fwd(y, ry, wl.dtype)
 
 
@@ -114,9 +117,13 @@ def test_bwd_other_ranks_many_chunks_and_tiles(R):
 
 
 @pytest.mark.parametrize("residual", [False, True])
-def test_bwd_residual_flag(residual):
-    wl = syn.Workload("tc_bwd_res", B=3, T=257, C=192, W=4, H=1, R=16, residual=residual)
-    run_bwd(wl, seed=4)
+@pytest.mark.parametrize("W,R", [(4, 16), (1, 16), (2, 16), (3, 16), (4, 32), (2, 32)])
+def test_bwd_residual_flag(residual, W, R):
+    # the residual flag is compiled into the backward: each (W, rank step)
+    # has a kernel with and one without it
+    wl = syn.Workload("tc_bwd_res", B=3, T=257, C=192, W=W, H=1, R=R, residual=residual,
+                      zu_std=R ** -0.5)
+    run_bwd(wl, seed=4 + W + R)
 
 
 @pytest.mark.parametrize("T", [1, 3, 4, 127, 128, 129, 131])
