@@ -448,3 +448,31 @@ def static_bwd(x, w, dy, residual=True, workspace=None):
         workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=x.device)
     dsc_static_bwd(x, w, dy, dx, dw, workspace, residual)
     return dx, dw
+
+
+def headwise_decode(x, w, state, H, residual=True):
+    """One decode step (x [B,C], w [B,C/H,W]); the state [B,W-1,C] is updated
+    in place.  Returns y [B,C]."""
+    y = torch.empty_like(x)
+    dsc_headwise_decode(x, w, state, y, H, residual)
+    return y
+
+
+def lowrank_decode(x, z, U, state, H, W, residual=True):
+    y = torch.empty_like(x)
+    dsc_lowrank_decode(x, z, U, state, y, H, W, residual)
+    return y
+
+
+def headwise_proj_decode(h, Wp, w, state, H, residual=True):
+    """Decode step merged with its projection x = h [B,D] Wp[C,D]^T; the state
+    is updated in place (its row 0 becomes x).  Returns y [B,C]."""
+    y = torch.empty(h.shape[0], Wp.shape[0], dtype=h.dtype, device=h.device)
+    dsc_headwise_proj_decode(h, Wp, w, state, y, H, residual)
+    return y
+
+
+def lowrank_proj_decode(h, Wp, z, U, state, H, W, residual=True):
+    y = torch.empty(h.shape[0], Wp.shape[0], dtype=h.dtype, device=h.device)
+    dsc_lowrank_proj_decode(h, Wp, z, U, state, y, H, W, residual)
+    return y

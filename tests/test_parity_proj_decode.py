@@ -138,3 +138,29 @@ def test_empty_batch_is_a_no_op():
                                  1, True)
     torch.cuda.synchronize()
     assert (y == 7.0).all()
+
+
+def test_convenience_functions_match_the_entry_points():
+    B, D, C, H, W, R = 3, 128, 64, 8, 4, 16
+    a = syn.proj_decode_inputs(B, D, C, H, W, 0, torch.bfloat16, seed=21, device="cuda")
+    b = syn.proj_decode_inputs(B, D, C, 1, W, R, torch.bfloat16, seed=22, device="cuda")
+    s1, s2 = a["state"].clone(), a["state"].clone()
+    y1 = dsc.headwise_proj_decode(a["h"], a["Wp"], a["w"], s1, H, True)
+    y2 = torch.empty_like(y1)
+    dsc.dsc_headwise_proj_decode(a["h"], a["Wp"], a["w"], s2, y2, H, True)
+    t1, t2 = b["state"].clone(), b["state"].clone()
+    z1 = dsc.lowrank_proj_decode(b["h"], b["Wp"], b["z"], b["U"], t1, 1, W, True)
+    z2 = torch.empty_like(z1)
+    dsc.dsc_lowrank_proj_decode(b["h"], b["Wp"], b["z"], b["U"], t2, z2, 1, W, True)
+    x = torch.randn(B, C, device="cuda").to(torch.bfloat16)
+    u1, u2 = a["state"].clone(), a["state"].clone()
+    d1 = dsc.headwise_decode(x, a["w"], u1, H, True)
+    d2 = torch.empty_like(d1)
+    dsc.dsc_headwise_decode(x, a["w"], u2, d2, H, True)
+    v1, v2 = b["state"].clone(), b["state"].clone()
+    e1 = dsc.lowrank_decode(x, b["z"], b["U"], v1, 1, W, True)
+    e2 = torch.empty_like(e1)
+    dsc.dsc_lowrank_decode(x, b["z"], b["U"], v2, e2, 1, W, True)
+    torch.cuda.synchronize()
+    for p, q in ((y1, y2), (s1, s2), (z1, z2), (t1, t2), (d1, d2), (u1, u2), (e1, e2), (v1, v2)):
+        assert torch.equal(p, q)
