@@ -622,7 +622,8 @@ def run_compare_decode(dev, steps, peak_gbs):
     dsc_headwise_proj_decode) next to the unmerged pair (the projection as a
     cuBLAS matmul writing x, then dsc_headwise_decode), at the decode shape
     of the QKV placement: hidden D = 2048, C = 6144 (q, k, v), H = 16, W = 4,
-    bf16, for B = 1, 4, 8, 16 and 64 sequences.  Eight layers' inputs (eight Wp of
+    bf16, for B = 1, 4, 8, 16, 32, 64 and 256 sequences (and the low-rank step,
+    R = 16, H = 1, for B = 1, 8 and 64).  Eight layers' inputs (eight Wp of
     25 MB: 201 MB, more than L2) are cycled, so each call reads its Wp from
     HBM as consecutive layers of a model do; the time per call is the event
     time of `steps` passes over the eight layers divided by the calls."""
@@ -630,7 +631,7 @@ def run_compare_decode(dev, steps, peak_gbs):
     dt = torch.bfloat16
     stream = torch.cuda.current_stream()
     res = {}
-    for B in (1, 4, 8, 16, 64):
+    for B in (1, 4, 8, 16, 32, 64, 256):
         layers = [syn.proj_decode_inputs(B, D, C, H, W, 0, dt, seed=10 + i, device=dev)
                   for i in range(NL)]
         x = torch.empty(B, C, dtype=dt, device=dev)
@@ -670,11 +671,50 @@ def run_compare_decode(dev, steps, peak_gbs):
                        "merged_gbs": round(gbs, 1),
                        "merged_frac_of_hbm_peak": round(gbs / peak_gbs, 4),
                        "bytes_per_call": nbytes}
+    # the low-rank step (R = 16, H = 1): taps z U formed in the kernel
+    res_lr = {}
+    R = 16
+    for B in (1, 8, 64):
+        layers = [syn.proj_decode_inputs(B, D, C, 1, W, R, dt, seed=40 + i, device=dev)
+                  for i in range(NL)]
+        x = torch.empty(B, C, dtype=dt, device=dev)
+        y = torch.empty(B, C, dtype=dt, device=dev)
+        fused = [dsc.bind("dsc_lowrank_proj_decode", L["h"], L["Wp"], L["z"], L["U"], L["state"],
+                          y, 1, W, True) for L in layers]
+        steps_ = [dsc.bind("dsc_lowrank_decode", x, L["z"], L["U"], L["state"], y, 1, W, True)
+                  for L in layers]
+
+        def run_fused_lr():
+            for f in fused:
+                f()
+
+        def run_unmerged_lr():
+            for L, f in zip(layers, steps_):
+                torch.mm(L["h"], L["Wp"].t(), out=x)
+                f()
+
+        out = {}
+        for name, f in (("merged", run_fused_lr), ("unmerged", run_unmerged_lr)):
+            for _ in range(3):
+                f()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(SPIN_CYCLES)
+            a.record(stream)
+            for _ in range(steps):
+                f()
+            b.record(stream)
+            torch.cuda.synchronize()
+            out[name] = a.elapsed_time(b) / (steps * NL) * 1e3
+        res_lr[str(B)] = {"merged_us": round(out["merged"], 2),
+                          "unmerged_us": round(out["unmerged"], 2),
+                          "speedup": round(out["unmerged"] / out["merged"], 3)}
     return {"comparison": "decode_step_merged_with_its_projection_vs_unmerged",
             "unit": "us_per_call", "kernel_launches_per_call": {"merged": 1, "unmerged": 2},
             "config": {"D": D, "C": C, "H": H, "W": W, "dtype": "bf16", "residual": True,
                        "layers_cycled": NL, "l2": "eight layers' weights (201 MB) cycled"},
-            "peak_gbs": peak_gbs, "B": res}
+            "peak_gbs": peak_gbs, "B": res,
+            "lowrank": {"config": {"R": R, "H": 1}, "B": res_lr}}
 
 
 def _time_calls(f, n, stream, flush):

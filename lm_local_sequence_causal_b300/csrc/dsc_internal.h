@@ -83,6 +83,13 @@ cudaError_t lowrank_bwd_tc(const void* x, const void* z, const void* U, const vo
 // Device error word of the tensor-core kernels (0 = no error; otherwise the
 // code of the bounded wait that gave up).  Synchronous; diagnostic only.
 cudaError_t lowrank_tc_error(unsigned int* out, bool reset);
+// The decode step merged with its projection on the tensor core (bf16,
+// W <= 4, R <= 32; any batch, in launches of up to 256 sequences).
+bool proj_decode_tc_supported(const Shape& s, int64_t D);
+cudaError_t proj_decode_tc(const void* h, const void* Wp, const void* w, const void* z,
+                           const void* U, void* state, void* y, const Shape& s, int64_t D,
+                           bool lowrank, cudaStream_t st);
+cudaError_t proj_decode_tc_error(unsigned int* out, bool reset);
 // Self-test of the failure path: the same kernels with every bounded wait
 // limited to wait_ns and a producer that issues no loads, so the waits of
 // the other roles run out; the kernels record a code in the error word, free

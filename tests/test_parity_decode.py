@@ -53,6 +53,42 @@ def test_lowrank_decode_step(dtype, W, R, H):
     assert torch.equal(state.double().cpu(), rstate)
 
 
+@pytest.mark.parametrize("dtype,B,C,H,W,R", [
+    # several passes of 32 (bf16) or 16 (fp32) sequences over one staged U
+    # slice; a partial last slice of 32 channels; H = 3 splits groups across
+    # slices, so some slices' columns start off a 16-byte boundary (element
+    # copies) and others on one (16-byte copies)
+    (torch.bfloat16, 40, 528, 3, 4, 16),
+    # U rows of 99 elements: every slice takes element copies
+    (torch.bfloat16, 70, 528, 16, 3, 7),
+    (torch.float32, 37, 36, 3, 4, 32),
+    (torch.float32, 5, 520, 1, 2, 16),
+    (torch.bfloat16, 33, 1048, 8, 4, 5),
+    (torch.bfloat16, 1, 6144, 1, 4, 16),
+    (torch.bfloat16, 8, 6144, 1, 4, 16),
+    (torch.bfloat16, 64, 6144, 1, 1, 32),
+])
+def test_lowrank_decode_blocks(dtype, B, C, H, W, R):
+    wl = syn.Workload("dec_lr_blk", B=B, T=1, C=C, W=W, H=H, R=R, dtype=dtype,
+                      zu_std=R ** -0.5)
+    inp = syn.make_inputs(wl, seed=B + C + R, device="cuda", need_grad_inputs=False)
+    x, z = inp["x"][:, 0].contiguous(), inp["z"][:, 0].contiguous()
+    st = Guarded((B, W - 1, C), dtype) if W > 1 else None
+    state = _state(B, W, C, dtype, 5)                  # [B, 0, C] when W = 1
+    if st is not None:
+        st.t.copy_(state)
+        state = st.t
+    ry, rstate = orc.lowrank_decode(x, z, inp["U"], state, H, W, True)
+    y = Guarded((B, C), dtype)
+    dsc.dsc_lowrank_decode(x, z, inp["U"], state, y.t, H, W, True)
+    torch.cuda.synchronize()
+    assert y.guards_intact()
+    assert_fwd(y.t, ry, dtype)
+    if st is not None:
+        assert st.guards_intact()
+        assert torch.equal(state.double().cpu(), rstate)
+
+
 def test_replay_matches_the_full_sequence_kernels():
     # head-wise QKV-like shape and low-rank, decoded token by token from a
     # zero state, against one call of the forward over the whole sequence

@@ -8,7 +8,8 @@ fp64, so a value next to a rounding boundary may land on the neighbouring
 bf16).  Every output sits in guard bands.  Also: a token-by-token replay
 against the full-sequence oracle, agreement with the unmerged pair
 (cuBLAS projection, then dsc_headwise_decode), the batch-block edges, the
-QKV decode shape, and B = 0."""
+QKV decode shape, the tcgen05 kernel's tiles, clusters and launches, and
+B = 0."""
 import pytest
 import torch
 
@@ -57,8 +58,9 @@ def test_headwise_step(dtype, W, H):
 
 @pytest.mark.parametrize("B", [1, 2, 3, 4, 5, 7, 8, 9, 16, 17, 31, 33, 64, 70])
 def test_batch_blocks(B):
-    # the CUDA-core kernel (1, 2 or 4 sequences per block; bf16 up to 4) and
-    # the tensor-core one (16, 32 or 64 per pass), partial blocks and passes
+    # the CUDA-core kernel (1, 2 or 4 sequences per block; bf16 up to 4), the
+    # warp-MMA one (16 per pass, up to 16 sequences) and the tcgen05 one
+    # (from 17), partial blocks and passes
     _run(torch.bfloat16, B=B, D=512, C=256, H=16, W=4, seed=B)
 
 
@@ -87,6 +89,25 @@ def test_lowrank_step(dtype, W, R, H, B):
 def test_qkv_decode_shape(B):
     # the QKV placement's decode step: D = 2048 hidden, C = 6144 = q, k, v
     _run(torch.bfloat16, B=B, D=2048, C=6144, H=16, W=4, seed=1)
+
+
+@pytest.mark.parametrize("B,D,C,H,W,R", [
+    (17, 512, 256, 16, 4, 0),      # the smallest batch on the tcgen05 kernel
+    (24, 512, 256, 16, 4, 0),
+    (24, 8, 136, 8, 3, 0),         # D of one short block; a partial 128-channel tile
+    (25, 1000, 1024, 1, 2, 0),     # a ragged last block of D; 8 tiles, wide clusters
+    (40, 6152, 128, 4, 1, 0),      # one tile, clusters of 8; W = 1
+    (256, 256, 384, 16, 4, 0),     # one full launch (N = 256)
+    (300, 128, 256, 2, 4, 0),      # two launches (256 + 44 sequences)
+    (24, 512, 256, 1, 4, 16),
+    (33, 1000, 520, 4, 3, 5),
+    (64, 2048, 6144, 16, 4, 0),    # the QKV decode shape
+    (64, 2048, 6144, 1, 4, 16),
+])
+def test_tensor_core_kernel(B, D, C, H, W, R):
+    # batches from 17 sequences take the tcgen05 kernel (D split over a
+    # cluster, partial sums added through distributed shared memory)
+    _run(torch.bfloat16, B=B, D=D, C=C, H=H, W=W, R=R, seed=B + D + W)
 
 
 def test_qkv_decode_shape_lowrank():
