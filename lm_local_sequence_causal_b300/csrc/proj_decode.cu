@@ -224,30 +224,26 @@ proj_decode_kernel(const T* __restrict__ h, const T* __restrict__ Wp, const T* _
 
 // ---------------------------------------------------------------------------
 // bf16: the projection on the warp-level tensor-core MMA (mma.sync m16n8k16,
-// bf16 in, fp32 accumulate).  A CTA owns NC = 8 NT output channels (NT
-// n-tiles of the MMA's N = 8) and its 4 warps split D: warp w takes the
-// 32-element chunks w, w+4, w+8, ...  Lane (g, q) = (lane / 4, lane % 4)
-// loads 16 bytes of Wp rows c0 + 8nt + g at offset 8q of a chunk and 16
-// bytes of h rows g and g+8 of a 16-sequence block (the MMA's M) at the same
-// offset; each h fragment feeds the NT tiles, so h, which every CTA reads
-// whole, is read C / NC times in all.  The contraction index may be
+// bf16 in, fp32 accumulate).  A CTA owns 8 output channels (the MMA's N) and
+// its 4 warps split D: warp w takes the 32-element chunks w, w+4, w+8, ...
+// Lane (g, q) = (lane / 4, lane % 4) loads 16 bytes of Wp row c0 + g at
+// offset 8q of a chunk and 16 bytes of h rows g and g+8 of a 16-sequence
+// block (the MMA's M) at the same offset.  The contraction index may be
 // ordered freely as long as both operands agree; here K slots 2q, 2q+1,
 // 2q+8, 2q+9 of MMA s (s = 0, 1) hold elements 8q + 4s + 0..3 of the chunk,
 // so each lane's 16-byte loads are its A and B fragments as they are.  The
 // four warps' partial sums meet in shared memory (added in warp order), and
-// thread t runs the decode steps of entries e = t + 128 i (i < NT) of each
-// 16-sequence block: sequence e / NC, channel c0 + e % NC.
+// thread t runs the decode step of sequence t / 8, channel c0 + t % 8.
 // Wp is read once per pass of up to 16*MB sequences (later passes from L2).
 // The tcgen05 MMA needs M >= 64 rows per CTA, i.e. 128 rows of Wp on M and
 // 48 CTAs at C = 6144, too few SMs to stream Wp at HBM speed without a
-// cross-CTA split of D; the warp-level MMA lets a CTA own 8 rows.
+// cross-CTA split of D; proj_decode_tc.cu makes that split for batches of
+// more than 16 sequences, and up to 16 this kernel, whose CTAs own 8 rows
+// and need no cross-CTA reduction, is as fast.
 
 constexpr int kMmaThreads = 128;   // 4 warps split D
-constexpr int kWpInFlight = 8;     // 16-byte Wp pieces in flight per lane
-// n-tiles of 8 channels per warp for 1, 2 and 4 blocks of 16 sequences
-constexpr int kNtMb1 = 1;
-constexpr int kNtMb2 = 2;
-constexpr int kNtMb4 = 2;
+constexpr int kMmaN = 8;           // output channels per CTA
+constexpr int kSeg = 8;            // chunks of a warp's Wp loads in flight
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
@@ -259,7 +255,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int W, bool LOWRANK, int MB, int NT>
+template <int W, bool LOWRANK, int MB>
 __global__ void __launch_bounds__(kMmaThreads)
 proj_decode_mma(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __restrict__ Wp,
                 const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ z,
@@ -267,67 +263,49 @@ proj_decode_mma(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __rest
                 __nv_bfloat16* __restrict__ y, int B, int D, int C, int H, int R,
                 int residual) {
   using T = __nv_bfloat16;
-  constexpr int NC = 8 * NT;                   // output channels per CTA
-  constexpr int SEG = kWpInFlight / NT;        // pieces of each Wp row in flight per lane
-  constexpr bool PRE = MB * NT <= 2;           // step operands fetched before the projection
-  static_assert(SEG >= 1 && SEG * NT == kWpInFlight, "NT must divide the pieces in flight");
-  __shared__ float part[4][MB][16][NC];
+  __shared__ float part[4][MB][16][kMmaN];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   const int nchunks = (D + 31) / 32;
-  const int nblk = (C + NC - 1) / NC;
+  const int nblk = (C + kMmaN - 1) / kMmaN;
+  // the (sequence, channel) of this thread's decode steps
+  const int m = threadIdx.x / kMmaN, n = threadIdx.x % kMmaN;
   for (int cb = blockIdx.x; cb < nblk; cb += gridDim.x) {
-    const int c0 = cb * NC;
-    bool row_ok[NT];
-    const T* wrow[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      row_ok[nt] = c0 + 8 * nt + g < C;
-      wrow[nt] = Wp + static_cast<int64_t>(c0 + 8 * nt + g) * D;
-    }
+    const int c0 = cb * kMmaN;
+    const bool row_ok = c0 + g < C;
+    const T* wrow = Wp + static_cast<int64_t>(c0 + g) * D;
+    const int c = c0 + n;
     for (int b0 = 0; b0 < B; b0 += 16 * MB) {
-      // Step operands of this thread's entries e = tid + 128 i of each
-      // 16-sequence block (sequence e / NC, channel e % NC).
-      T tap_raw[PRE ? MB : 1][PRE ? NT : 1][LOWRANK ? 1 : W];
-      T sr[PRE ? MB : 1][PRE ? NT : 1][W > 1 ? W - 1 : 1];
-      if constexpr (PRE) {
+      // Step operands of this thread, fetched before the projection.
+      T tap_raw[MB][LOWRANK ? 1 : W];
+      T sr[MB][W > 1 ? W - 1 : 1];
 #pragma unroll
-        for (int mb = 0; mb < MB; ++mb)
+      for (int mb = 0; mb < MB; ++mb) {
+        const int64_t bg = b0 + 16 * mb + m;
+        if (bg < B && c < C) {
+          if constexpr (!LOWRANK) {
+            const T* wb = w + (bg * (C / H) + c / H) * W;
 #pragma unroll
-          for (int i = 0; i < NT; ++i) {
-            const int e = threadIdx.x + kMmaThreads * i;
-            const int64_t bg = b0 + 16 * mb + e / NC;
-            const int c = c0 + e % NC;
-            if (bg < B && c < C) {
-              if constexpr (!LOWRANK) {
-                const T* wb = w + (bg * (C / H) + c / H) * W;
-#pragma unroll
-                for (int k = 0; k < W; ++k) tap_raw[mb][i][k] = wb[k];
-              }
-              if constexpr (W > 1) {
-                const T* sp = state + bg * (W - 1) * C + c;
-#pragma unroll
-                for (int j = 0; j < W - 1; ++j) sr[mb][i][j] = sp[static_cast<int64_t>(j) * C];
-              }
-            }
+            for (int k = 0; k < W; ++k) tap_raw[mb][k] = wb[k];
           }
+          if constexpr (W > 1) {
+            const T* sp = state + bg * (W - 1) * C + c;
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j) sr[mb][j] = sp[static_cast<int64_t>(j) * C];
+          }
+        }
       }
-      float acc[MB][NT][4];
+      float acc[MB][4];
 #pragma unroll
       for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int i = 0; i < 4; ++i) acc[mb][i] = 0.f;
+      for (int j0 = warp; j0 < nchunks; j0 += 4 * kSeg) {
+        uint4 wq[kSeg];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc[mb][nt][i] = 0.f;
-      for (int j0 = warp; j0 < nchunks; j0 += 4 * SEG) {
-        uint4 wq[NT][SEG];
-#pragma unroll
-        for (int sg = 0; sg < SEG; ++sg) {
+        for (int sg = 0; sg < kSeg; ++sg) {
           const int d = 32 * (j0 + 4 * sg) + 8 * q;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            wq[nt][sg] = (row_ok[nt] && d < D) ? ldg16_stream(wrow[nt] + d)
-                                               : make_uint4(0u, 0u, 0u, 0u);
+          wq[sg] = (row_ok && d < D) ? ldg16_stream(wrow + d) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int mb = 0; mb < MB; ++mb) {
@@ -335,105 +313,77 @@ proj_decode_mma(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __rest
           const T* h0p = h + static_cast<int64_t>(r0) * D;
           const T* h1p = h + static_cast<int64_t>(r1) * D;
 #pragma unroll
-          for (int sg = 0; sg < SEG; ++sg) {
+          for (int sg = 0; sg < kSeg; ++sg) {
             if (j0 + 4 * sg >= nchunks) break;              // the same for the whole warp
             const int d = 32 * (j0 + 4 * sg) + 8 * q;
             const uint4 h0 = (r0 < B && d < D) ? ldg16(h0p + d) : make_uint4(0u, 0u, 0u, 0u);
             const uint4 h1 = (r1 < B && d < D) ? ldg16(h1p + d) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              mma_bf16_16816(acc[mb][nt], h0.x, h1.x, h0.y, h1.y, wq[nt][sg].x, wq[nt][sg].y);
-              mma_bf16_16816(acc[mb][nt], h0.z, h1.z, h0.w, h1.w, wq[nt][sg].z, wq[nt][sg].w);
-            }
+            mma_bf16_16816(acc[mb], h0.x, h1.x, h0.y, h1.y, wq[sg].x, wq[sg].y);
+            mma_bf16_16816(acc[mb], h0.z, h1.z, h0.w, h1.w, wq[sg].z, wq[sg].w);
           }
         }
       }
-      // D fragment of tile nt: (row g, cols 8nt + 2q, +1) and (row g+8, the same)
+      // D fragment: (row g, cols 2q, 2q+1) and (row g+8, cols 2q, 2q+1)
 #pragma unroll
-      for (int mb = 0; mb < MB; ++mb)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          part[warp][mb][g][8 * nt + 2 * q] = acc[mb][nt][0];
-          part[warp][mb][g][8 * nt + 2 * q + 1] = acc[mb][nt][1];
-          part[warp][mb][g + 8][8 * nt + 2 * q] = acc[mb][nt][2];
-          part[warp][mb][g + 8][8 * nt + 2 * q + 1] = acc[mb][nt][3];
-        }
+      for (int mb = 0; mb < MB; ++mb) {
+        part[warp][mb][g][2 * q] = acc[mb][0];
+        part[warp][mb][g][2 * q + 1] = acc[mb][1];
+        part[warp][mb][g + 8][2 * q] = acc[mb][2];
+        part[warp][mb][g + 8][2 * q + 1] = acc[mb][3];
+      }
       __syncthreads();
 #pragma unroll
-      for (int mb = 0; mb < MB; ++mb)
+      for (int mb = 0; mb < MB; ++mb) {
+        const int64_t bg = b0 + 16 * mb + m;
+        if (bg >= B || c >= C) continue;
+        const float xsum = ((part[0][mb][m][n] + part[1][mb][m][n]) + part[2][mb][m][n]) +
+                           part[3][mb][m][n];
+        const T xs = from_f32<T>(xsum);    // x_t as the projection would store it
+        const float xf = to_f32(xs);
+        float taps[W];
+        if constexpr (!LOWRANK) {
 #pragma unroll
-        for (int i = 0; i < NT; ++i) {
-          const int e = threadIdx.x + kMmaThreads * i;
-          const int m = e / NC, n = e % NC;
-          const int64_t bg = b0 + 16 * mb + m;
-          const int c = c0 + n;
-          if (bg >= B || c >= C) continue;
-          const float xsum = ((part[0][mb][m][n] + part[1][mb][m][n]) + part[2][mb][m][n]) +
-                             part[3][mb][m][n];
-          const T xs = from_f32<T>(xsum);    // x_t as the projection would store it
-          const float xf = to_f32(xs);
-          float taps[W];
-          if constexpr (!LOWRANK) {
-            if constexpr (PRE) {
+          for (int k = 0; k < W; ++k) taps[k] = to_f32(tap_raw[mb][k]);
+        } else {
+          const int64_t GW = static_cast<int64_t>(C / H) * W;
+          const int64_t gg = c / H;
 #pragma unroll
-              for (int k = 0; k < W; ++k) taps[k] = to_f32(tap_raw[mb][i][k]);
-            } else {
-              const T* wb = w + (bg * (C / H) + c / H) * W;
-#pragma unroll
-              for (int k = 0; k < W; ++k) taps[k] = to_f32(wb[k]);
-            }
-          } else {
-            const int64_t GW = static_cast<int64_t>(C / H) * W;
-            const int64_t gg = c / H;
-#pragma unroll
-            for (int k = 0; k < W; ++k) taps[k] = 0.f;
+          for (int k = 0; k < W; ++k) taps[k] = 0.f;
 #pragma unroll 8
-            for (int rr = 0; rr < R; ++rr) {
-              const float zr = to_f32(z[bg * R + rr]);
-              const T* ur = U + rr * GW + gg * W;
+          for (int rr = 0; rr < R; ++rr) {
+            const float zr = to_f32(z[bg * R + rr]);
+            const T* ur = U + rr * GW + gg * W;
 #pragma unroll
-              for (int k = 0; k < W; ++k) taps[k] = fmaf(zr, to_f32(ur[k]), taps[k]);
-            }
+            for (int k = 0; k < W; ++k) taps[k] = fmaf(zr, to_f32(ur[k]), taps[k]);
           }
-          float a = residual ? xf : 0.f;
-          a = fmaf(taps[0], xf, a);
-          if constexpr (W > 1) {
-            T* sp = state + bg * (W - 1) * C + c;
-            T sv[W - 1];
-            if constexpr (PRE) {
-#pragma unroll
-              for (int j = 0; j < W - 1; ++j) sv[j] = sr[mb][i][j];
-            } else {
-#pragma unroll
-              for (int j = 0; j < W - 1; ++j) sv[j] = sp[static_cast<int64_t>(j) * C];
-            }
-#pragma unroll
-            for (int k = 1; k < W; ++k) a = fmaf(taps[k], to_f32(sv[k - 1]), a);
-#pragma unroll
-            for (int j = W - 2; j >= 1; --j) sp[static_cast<int64_t>(j) * C] = sv[j - 1];
-            sp[0] = xs;
-          }
-          y[bg * C + c] = from_f32<T>(a);
         }
+        float a = residual ? xf : 0.f;
+        a = fmaf(taps[0], xf, a);
+        if constexpr (W > 1) {
+          T* sp = state + bg * (W - 1) * C + c;
+#pragma unroll
+          for (int k = 1; k < W; ++k) a = fmaf(taps[k], to_f32(sr[mb][k - 1]), a);
+#pragma unroll
+          for (int j = W - 2; j >= 1; --j) sp[static_cast<int64_t>(j) * C] = sr[mb][j - 1];
+          sp[0] = xs;
+        }
+        y[bg * C + c] = from_f32<T>(a);
+      }
       __syncthreads();                       // part is rewritten by the next pass
     }
   }
 }
-
-// Channels per CTA (8 NT) by the 16-sequence blocks per pass: every CTA
-// reads all of h for its pass, so wider CTAs read h fewer times.
-template <int MB>
-struct MmaNt {
-  static constexpr int value = MB == 1 ? kNtMb1 : MB == 2 ? kNtMb2 : kNtMb4;
-};
 
 template <bool LOWRANK>
 cudaError_t launch_mma(const void* h, const void* Wp, const void* w, const void* z,
                        const void* U, void* state, void* y, const Shape& s, int64_t D,
                        cudaStream_t st) {
   using T = __nv_bfloat16;
+  const int64_t nblk = (s.C + kMmaN - 1) / kMmaN;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
+  const unsigned g =
+      static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(nblk, int64_t(sms) * 16)));
   const int B = static_cast<int>(s.B), Di = static_cast<int>(D), C = static_cast<int>(s.C),
             H = static_cast<int>(s.H), R = static_cast<int>(s.R);
   const T* ph = static_cast<const T*>(h);
@@ -443,23 +393,12 @@ cudaError_t launch_mma(const void* h, const void* Wp, const void* w, const void*
   const T* pU = static_cast<const T*>(U);
   T* ps = static_cast<T*>(state);
   T* py = static_cast<T*>(y);
-  // 16-sequence blocks per pass: the batch rounded up to 16, 32 or 64.
-  const int mb = s.B <= 16 ? 1 : s.B <= 32 ? 2 : 4;
-#define DSC_PDM_LAUNCH(Wv, MBv)                                                             \
-  do {                                                                                      \
-    constexpr int NTv = MmaNt<MBv>::value;                                                  \
-    const int64_t nblk = (s.C + 8 * NTv - 1) / (8 * NTv);                                   \
-    const unsigned g = static_cast<unsigned>(                                               \
-        std::max<int64_t>(1, std::min<int64_t>(nblk, int64_t(sms) * 16)));                 \
-    proj_decode_mma<Wv, LOWRANK, MBv, NTv><<<g, kMmaThreads, 0, st>>>(                      \
-        ph, pW, pw, pz, pU, ps, py, B, Di, C, H, R, s.residual);                            \
-  } while (0)
-#define DSC_PDM_MB(Wv)                    \
-  switch (mb) {                           \
-    case 1: DSC_PDM_LAUNCH(Wv, 1); break; \
-    case 2: DSC_PDM_LAUNCH(Wv, 2); break; \
-    default: DSC_PDM_LAUNCH(Wv, 4); break; \
-  }
+  // One 16-sequence block per pass: batches of more than 16 sequences take
+  // the tcgen05 kernel (proj_decode_tc.cu), so a call here has one pass.
+#define DSC_PDM_LAUNCH(Wv, MBv)                                                                 \
+  proj_decode_mma<Wv, LOWRANK, MBv><<<g, kMmaThreads, 0, st>>>(ph, pW, pw, pz, pU, ps, py, B, \
+                                                              Di, C, H, R, s.residual)
+#define DSC_PDM_MB(Wv) DSC_PDM_LAUNCH(Wv, 1)
   switch (s.W) {
     case 1: DSC_PDM_MB(1); break;
     case 2: DSC_PDM_MB(2); break;
