@@ -311,6 +311,24 @@ dsc_status_t dsc_lowrank_bwd_selftest_timeout(
     dsc_dtype_t dtype, uint64_t wait_limit_ns, void* stream);
 
 /*
+ * Self-test of the failure path of the tcgen05 kernel behind
+ * dsc_headwise_proj_decode (bf16 batches of 17 or more sequences; its CTAs
+ * form clusters that meet at cluster barriers).  As above: every bounded
+ * wait limited to wait_limit_ns (1 us .. 1 s) and a producer that issues no
+ * loads, so the MMA issuer's wait runs out; every CTA still reaches both
+ * cluster barriers, frees its TMEM and returns.  Expected result: DSC_OK,
+ * then dsc_device_error reports 2 (or 3), y and state are unspecified, and
+ * the next normal call runs correctly.  Arguments as for
+ * dsc_headwise_proj_decode plus wait_limit_ns; DSC_ERR_UNSUPPORTED when the
+ * call would not take the tcgen05 kernel (fp32, or fewer than 17
+ * sequences), DSC_ERR_INVALID_ARG for B = 0 or a limit outside the range.
+ */
+dsc_status_t dsc_headwise_proj_decode_selftest_timeout(
+    const void* h, const void* Wp, const void* w, void* state, void* y, int64_t B, int64_t D,
+    int64_t C, int64_t H, int64_t W, int residual, dsc_dtype_t dtype, uint64_t wait_limit_ns,
+    void* stream);
+
+/*
  * Largest workspace dsc_lowrank_bwd_noalloc can provide: 32 MiB.
  */
 #define DSC_LOWRANK_BWD_NOALLOC_MAX_BYTES ((size_t)32 << 20)

@@ -198,6 +198,25 @@ dsc_status_t dsc_headwise_proj_decode(const void* h, const void* Wp, const void*
                                              (cudaStream_t)stream));
 }
 
+dsc_status_t dsc_headwise_proj_decode_selftest_timeout(const void* h, const void* Wp,
+                                                      const void* w, void* state, void* y,
+                                                      int64_t B, int64_t D, int64_t C, int64_t H,
+                                                      int64_t W, int residual, dsc_dtype_t dtype,
+                                                      uint64_t wait_limit_ns, void* stream) {
+  dsc_status_t st = check_shape(B, 1, C, H, W, 0, dtype, false);
+  if (st != DSC_OK) return st;
+  if ((st = check_proj(B, D, dtype)) != DSC_OK) return st;
+  if (B == 0 || wait_limit_ns < 1000 || wait_limit_ns > 1000000000ull) return DSC_ERR_INVALID_ARG;
+  const Shape s = make_shape(B, 1, C, H, W, 0, residual, dtype);
+  if (!dsc::headwise_proj_decode_uses_tc(s, D)) return DSC_ERR_UNSUPPORTED;
+  if ((st = check_ptrs({h, Wp, w, y})) != DSC_OK) return st;
+  if (W > 1 && (st = check_ptrs({state})) != DSC_OK) return st;
+  if (y == h || y == Wp || (W > 1 && (state == h || state == y || state == Wp)))
+    return DSC_ERR_INVALID_ARG;
+  return from_cuda(dsc::proj_decode_tc_selftest(h, Wp, w, state, y, s, D, wait_limit_ns,
+                                                (cudaStream_t)stream));
+}
+
 dsc_status_t dsc_lowrank_proj_decode(const void* h, const void* Wp, const void* z, const void* U,
                                      void* state, void* y, int64_t B, int64_t D, int64_t C,
                                      int64_t H, int64_t W, int64_t R, int residual,

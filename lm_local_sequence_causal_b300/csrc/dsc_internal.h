@@ -90,6 +90,13 @@ cudaError_t proj_decode_tc(const void* h, const void* Wp, const void* w, const v
                            const void* U, void* state, void* y, const Shape& s, int64_t D,
                            bool lowrank, cudaStream_t st);
 cudaError_t proj_decode_tc_error(unsigned int* out, bool reset);
+// Failure-path self-test of the head-wise tcgen05 kernel: waits limited to
+// wait_ns and a producer that issues no loads.
+cudaError_t proj_decode_tc_selftest(const void* h, const void* Wp, const void* w, void* state,
+                                    void* y, const Shape& s, int64_t D, uint64_t wait_ns,
+                                    cudaStream_t st);
+// Whether dsc_headwise_proj_decode takes the tcgen05 kernel for this shape.
+bool headwise_proj_decode_uses_tc(const Shape& s, int64_t D);
 // Self-test of the failure path: the same kernels with every bounded wait
 // limited to wait_ns and a producer that issues no loads, so the waits of
 // the other roles run out; the kernels record a code in the error word, free

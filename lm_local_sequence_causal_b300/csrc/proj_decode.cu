@@ -468,6 +468,10 @@ constexpr int64_t kTcMinB = 17;
 
 }  // namespace
 
+bool headwise_proj_decode_uses_tc(const Shape& s, int64_t D) {
+  return s.bf16 && s.B >= kTcMinB && proj_decode_tc_supported(s, D);
+}
+
 cudaError_t headwise_proj_decode(const void* h, const void* Wp, const void* w, void* state,
                                  void* y, const Shape& s, int64_t D, cudaStream_t st) {
   if (s.bf16 && s.B >= kTcMinB && proj_decode_tc_supported(s, D))

@@ -72,6 +72,7 @@ struct PdtArgs {
   int nkb;                     // 64-element blocks of D
   int nst;                     // pipeline stages
   unsigned long long wns;      // wait limit
+  int withhold;                // self-test: the producer issues no loads, so waits run out
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -213,7 +214,7 @@ proj_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_wp,
       const uint64_t pol_wp = policy_evict_first();   // read once
       const uint64_t pol_h = policy_evict_last();     // read by every tile
       int i = 0;
-      for (; i < nk; ++i) {
+      for (; i < nk && !a.withhold; ++i) {
         const int s = i % a.nst;
         const uint32_t ph = (i / a.nst) & 1;
         if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_pd_error, 1, a.wns)) break;
@@ -491,7 +492,8 @@ int max_clusters(int ks) {
 
 template <int W, bool LOWRANK>
 cudaError_t run_w(const void* h, const void* Wp, const void* w, const void* z, const void* U,
-                  void* state, void* y, const Shape& s, int64_t D, cudaStream_t st) {
+                  void* state, void* y, const Shape& s, int64_t D, cudaStream_t st,
+                  uint64_t wait_ns, int withhold) {
   using T = __nv_bfloat16;
   auto kern = proj_decode_tc_kernel<W, LOWRANK>;
   cudaError_t e = set_smem<PdtKernelTag<W, LOWRANK>>(kern, kPdtSmem);
@@ -534,7 +536,8 @@ cudaError_t run_w(const void* h, const void* Wp, const void* w, const void* z, c
     a.R = static_cast<int>(s.R);
     a.residual = s.residual;
     a.nkb = nkb;
-    a.wns = kWaitLimitNs;
+    a.wns = wait_ns;
+    a.withhold = withhold;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     cluster_config(cfg, attr, static_cast<unsigned>(ntile * ks), static_cast<unsigned>(ks), smem,
@@ -552,13 +555,15 @@ bool proj_decode_tc_supported(const Shape& s, int64_t D) {
          s.C <= (int64_t(1) << 24) && s.B >= 1;
 }
 
-cudaError_t proj_decode_tc(const void* h, const void* Wp, const void* w, const void* z,
-                           const void* U, void* state, void* y, const Shape& s, int64_t D,
-                           bool lowrank, cudaStream_t st) {
+namespace {
+
+cudaError_t run(const void* h, const void* Wp, const void* w, const void* z, const void* U,
+                void* state, void* y, const Shape& s, int64_t D, bool lowrank, cudaStream_t st,
+                uint64_t wait_ns, int withhold) {
   if (!proj_decode_tc_supported(s, D)) return cudaErrorNotSupported;
-#define DSC_PDT_W(Wv)                                                          \
-  return lowrank ? run_w<Wv, true>(h, Wp, w, z, U, state, y, s, D, st)        \
-                 : run_w<Wv, false>(h, Wp, w, z, U, state, y, s, D, st)
+#define DSC_PDT_W(Wv)                                                                         \
+  return lowrank ? run_w<Wv, true>(h, Wp, w, z, U, state, y, s, D, st, wait_ns, withhold)    \
+                 : run_w<Wv, false>(h, Wp, w, z, U, state, y, s, D, st, wait_ns, withhold)
   switch (s.W) {
     case 1: DSC_PDT_W(1);
     case 2: DSC_PDT_W(2);
@@ -566,6 +571,20 @@ cudaError_t proj_decode_tc(const void* h, const void* Wp, const void* w, const v
     default: DSC_PDT_W(4);
   }
 #undef DSC_PDT_W
+}
+
+}  // namespace
+
+cudaError_t proj_decode_tc(const void* h, const void* Wp, const void* w, const void* z,
+                           const void* U, void* state, void* y, const Shape& s, int64_t D,
+                           bool lowrank, cudaStream_t st) {
+  return run(h, Wp, w, z, U, state, y, s, D, lowrank, st, kWaitLimitNs, 0);
+}
+
+cudaError_t proj_decode_tc_selftest(const void* h, const void* Wp, const void* w, void* state,
+                                    void* y, const Shape& s, int64_t D, uint64_t wait_ns,
+                                    cudaStream_t st) {
+  return run(h, Wp, w, nullptr, nullptr, state, y, s, D, false, st, wait_ns, 1);
 }
 
 cudaError_t proj_decode_tc_error(unsigned int* out, bool reset) {

@@ -74,6 +74,9 @@ def load():
     lib.dsc_lowrank_proj_decode.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, I64, I64,
                                             INT, INT, P]
     lib.dsc_lowrank_proj_decode.restype = INT
+    lib.dsc_headwise_proj_decode_selftest_timeout.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
+                                                              I64, INT, INT, ctypes.c_uint64, P]
+    lib.dsc_headwise_proj_decode_selftest_timeout.restype = INT
     lib.dsc_lowrank_uses_tensor_cores.argtypes = [I64, I64, I64, I64, I64, I64, INT]
     lib.dsc_lowrank_uses_tensor_cores.restype = INT
     lib.dsc_headwise_uses_tma.argtypes = [I64, I64, I64, I64, I64, INT]
@@ -346,6 +349,16 @@ def dsc_static_bwd_workspace_size(B, T, C, W, dtype) -> int:
 def dsc_static_bwd(x, w, dy, dx, dw, workspace, residual=True, stream=None):
     """dx [B,T,C] and dw [C,W] of the static short conv; `workspace` is a uint8 CUDA tensor."""
     _call("dsc_static_bwd", _m_dsc_static_bwd(x, w, dy, dx, dw, workspace, residual, stream))
+
+
+def dsc_headwise_proj_decode_selftest_timeout(h, Wp, w, state, y, H, wait_limit_ns,
+                                              residual=True, stream=None):
+    """Failure-path self-test of the tcgen05 merged decode kernel (bf16, 17 or
+    more sequences): waits limited to wait_limit_ns and no loads issued; read
+    the code with dsc_device_error() afterwards.  y and state are left
+    unspecified."""
+    a = _m_dsc_headwise_proj_decode(h, Wp, w, state, y, H, residual, stream)
+    _call("dsc_headwise_proj_decode_selftest_timeout", a[:-1] + (int(wait_limit_ns), a[-1]))
 
 
 def dsc_lowrank_fwd_selftest_timeout(x, z, U, y, H, W, wait_limit_ns, residual=True,

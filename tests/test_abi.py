@@ -192,6 +192,27 @@ def test_selftest_entry_points_validate_on_the_host(lib):
              16, 1, BF16, u64(10), None) == dsc.DSC_ERR_INVALID_ARG
 
 
+def test_proj_decode_selftest_validates_on_the_host(lib):
+    # (h, Wp, w, state, y, B, D, C, H, W, residual, dtype, limit)
+    f = lib.dsc_headwise_proj_decode_selftest_timeout
+    u64 = ctypes.c_uint64
+    ok_limit = u64(2_000_000)
+    for lim in (0, 999, 2_000_000_000):
+        assert f(A, A2, A3, A4, A5, 24, 1024, 1024, 16, 4, 1, BF16, u64(lim), None) == \
+            dsc.DSC_ERR_INVALID_ARG
+    assert f(A, A2, A3, A4, A5, 0, 1024, 1024, 16, 4, 1, BF16, ok_limit, None) == \
+        dsc.DSC_ERR_INVALID_ARG
+    # fewer than 17 sequences, or fp32: not the tcgen05 kernel
+    assert f(A, A2, A3, A4, A5, 16, 1024, 1024, 16, 4, 1, BF16, ok_limit, None) == \
+        dsc.DSC_ERR_UNSUPPORTED
+    assert f(A, A2, A3, A4, A5, 24, 1024, 1024, 16, 4, 1, F32, ok_limit, None) == \
+        dsc.DSC_ERR_UNSUPPORTED
+    assert f(A, MIS, A3, A4, A5, 24, 1024, 1024, 16, 4, 1, BF16, ok_limit, None) == \
+        dsc.DSC_ERR_ALIGNMENT
+    assert f(A, A2, A3, A4, A, 24, 1024, 1024, 16, 4, 1, BF16, ok_limit, None) == \
+        dsc.DSC_ERR_INVALID_ARG                                               # y aliases h
+
+
 def test_proj_decode_validation(lib):
     # (h, Wp, w, state, y, B, D, C, H, W, residual, dtype)
     f = lib.dsc_headwise_proj_decode

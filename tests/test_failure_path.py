@@ -1,5 +1,5 @@
-"""Failure path of the tensor-core low-rank kernels, exercised without a GPU
-fault.
+"""Failure path of the tensor-core low-rank kernels and of the tcgen05
+merged decode kernel, exercised without a GPU fault.
 
 Every wait of those kernels on an mbarrier is bounded: when it runs out the
 waiting role records a code in the device error word, raises the CTA's abort
@@ -80,6 +80,40 @@ def test_backward_wait_timeout_is_reported_and_the_device_recovers():
     assert code in WAIT_CODES, f"error word {code}"
     assert elapsed < 5.0, f"the kernels took {elapsed:.2f} s to give up"
     check_normal_call_after(wl, inp)
+
+
+def test_merged_decode_cluster_kernel_times_out_and_the_device_recovers():
+    # the tcgen05 merged decode: CTAs in clusters of 2 to 8 that meet at two
+    # cluster barriers; with no loads issued the MMA issuer's wait runs out,
+    # and every CTA must still pass both barriers and free its TMEM
+    B, D, C, H, W = 24, 1024, 1024, 16, 4
+    inp = syn.proj_decode_inputs(B, D, C, H, W, 0, torch.bfloat16, seed=6, device="cuda")
+    y = torch.empty(B, C, dtype=torch.bfloat16, device="cuda")
+    st = inp["state"].clone()
+    torch.cuda.synchronize()
+    dsc.dsc_device_error(reset=True)
+    t0 = time.perf_counter()
+    dsc.dsc_headwise_proj_decode_selftest_timeout(inp["h"], inp["Wp"], inp["w"], st, y, H,
+                                                  LIMIT_NS)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    code = dsc.dsc_device_error(reset=True)
+    assert code in WAIT_CODES, f"error word {code}"
+    assert elapsed < 5.0, f"the kernel took {elapsed:.2f} s to give up"
+    # a normal call on the same device afterwards
+    st0 = inp["state"].clone()
+    ry, rstate, _ = orc.headwise_proj_decode(inp["h"], inp["Wp"], inp["w"], st0, H, True)
+    st = inp["state"].clone()
+    dsc.dsc_headwise_proj_decode(inp["h"], inp["Wp"], inp["w"], st, y, H, True)
+    torch.cuda.synchronize()
+    assert dsc.dsc_device_error() == 0
+    assert_fwd(y, ry, torch.bfloat16)
+    assert torch.equal(st[:, 1:].double().cpu(), rstate[:, 1:])
+    # shapes that do not take the tcgen05 kernel have no self-test
+    with pytest.raises(dsc.DSCError) as e:
+        dsc.dsc_headwise_proj_decode_selftest_timeout(inp["h"][:8], inp["Wp"], inp["w"][:8],
+                                                      st[:8], y[:8], H, LIMIT_NS)
+    assert e.value.status == dsc.DSC_ERR_UNSUPPORTED
 
 
 def test_selftest_rejects_bad_limits_and_non_tensor_core_shapes():
