@@ -17,8 +17,9 @@
 // rows) straight into the tensor core's layout, and the fp32 accumulator
 // lives in TMEM (128 lanes = channels, N columns = sequences).  C / 128
 // channel tiles alone would leave most SMs idle (48 at C = 6144), so D is
-// split over a cluster of KS CTAs (KS ~ SMs / tiles, at most 8): rank q
-// takes a contiguous range of D's 64-element blocks.  The KS partial tiles
+// split over a cluster of KS CTAs (the largest KS <= 8 whose clusters all
+// fit on the device at once): rank q takes a contiguous range of D's
+// 64-element blocks.  The KS partial tiles
 // meet through distributed shared memory: rank q finishes the sequences
 // b = q, q + KS, ... of the tile, so every rank stores its partial sums of
 // those sequences into rank q's shared memory (stores, which do not stall
@@ -28,9 +29,10 @@
 // state and y are contiguous along the channels.
 //
 // Roles (8 warps): warp 0 lane 0 issues the TMA loads of a ring of stages,
-// warp 1 owns TMEM and lane 0 issues the MMAs; after the K loop all eight
-// warps (warps w and w + 4 read TMEM lanes 32w..32w+31, one half of the
-// columns each) run the epilogue.  Every mbarrier wait is bounded in time (a
+// warp 1 owns TMEM and lane 0 issues the MMAs, warps 2-7 prefetch the
+// decode step's operands into L2; after the K loop all eight warps run the
+// epilogue (warps w and w + 4 read TMEM lanes 32 (w mod 4) .. + 31 and take
+// alternate chunks of columns).  Every mbarrier wait is bounded in time (a
 // broken pipeline sets an error code and the kernel returns); both cluster
 // barriers are reached by every thread of every CTA whatever happened before
 // them, so no CTA waits on one that left.
@@ -52,7 +54,7 @@ using namespace sm100;
 
 __device__ unsigned int g_pd_error = 0;
 
-constexpr int kPdtThreads = 256;       // 8 warps; warps 0 and 1 also load and issue
+constexpr int kPdtThreads = 256;            // 8 warps
 constexpr int kPdtM = 128;                  // channels per CTA (the MMA's M)
 constexpr int kPdtMaxN = 256;               // sequences per launch (the MMA's N)
 constexpr int kPdtMaxStages = 8;
