@@ -72,6 +72,12 @@ def test_hidden_sizes(D, B):
     _run(torch.bfloat16, B=B, D=D, C=128, H=8, W=3, seed=D + B)
 
 
+@pytest.mark.parametrize("B", [9, 40])
+def test_fp32_batches(B):
+    # fp32 always takes the CUDA-core kernel: blocks of 8 sequences, passes
+    _run(torch.float32, B=B, D=200, C=264, H=8, W=4, seed=B)
+
+
 @pytest.mark.parametrize("residual", [False, True])
 def test_residual_switch(residual):
     _run(torch.bfloat16, B=4, D=128, C=64, H=1, W=4, residual=residual, seed=7)
@@ -103,6 +109,8 @@ def test_qkv_decode_shape(B):
     (33, 1000, 520, 4, 3, 5),
     (64, 2048, 6144, 16, 4, 0),    # the QKV decode shape
     (64, 2048, 6144, 1, 4, 16),
+    (20, 256, 384, 3, 4, 0),       # groups of 3 straddle the 128-channel tiles
+    (18, 136, 264, 3, 2, 7),       # the same for tied low-rank filters; partial tile
 ])
 def test_tensor_core_kernel(B, D, C, H, W, R):
     # batches from 17 sequences take the tcgen05 kernel (D split over a
