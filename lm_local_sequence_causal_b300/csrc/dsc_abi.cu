@@ -285,11 +285,12 @@ int dsc_lowrank_uses_tensor_cores(int64_t B, int64_t T, int64_t C, int64_t H, in
 
 dsc_status_t dsc_device_error(unsigned int* code, int reset) {
   if (code == nullptr) return DSC_ERR_INVALID_ARG;
-  unsigned int a = 0, b = 0, c = 0;
+  unsigned int a = 0, b = 0, c = 0, d = 0;
   cudaError_t e = dsc::lowrank_tc_error(&a, reset != 0);
   if (e == cudaSuccess) e = dsc::headwise_tma_error(&b, reset != 0);
   if (e == cudaSuccess) e = dsc::proj_decode_tc_error(&c, reset != 0);
-  *code = a != 0 ? a : b != 0 ? b : c;
+  if (e == cudaSuccess) e = dsc::static_tma_error(&d, reset != 0);
+  *code = a != 0 ? a : b != 0 ? b : c != 0 ? c : d;
   return from_cuda(e);
 }
 

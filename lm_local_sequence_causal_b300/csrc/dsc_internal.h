@@ -90,6 +90,8 @@ cudaError_t proj_decode_tc(const void* h, const void* Wp, const void* w, const v
                            const void* U, void* state, void* y, const Shape& s, int64_t D,
                            bool lowrank, cudaStream_t st);
 cudaError_t proj_decode_tc_error(unsigned int* out, bool reset);
+// Device error word of the TMA-staged static backward.
+cudaError_t static_tma_error(unsigned int* out, bool reset);
 // Failure-path self-test of the head-wise tcgen05 kernel: waits limited to
 // wait_ns and a producer that issues no loads.
 cudaError_t proj_decode_tc_selftest(const void* h, const void* Wp, const void* w, void* state,

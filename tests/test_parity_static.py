@@ -66,6 +66,37 @@ def test_static_large_sampled(dtype):
     assert_grad(dw, rdw, dtype, "dw")
 
 
+# bf16 with C a multiple of 64 takes the TMA-staged kernels: one CTA per
+# (64-channel chunk, part of the chunk's 128-token tiles).  (3, 300, 384):
+# 9 tiles (a partial one per sequence), one tile per CTA, so the second
+# epilogue group of every CTA has no tile and contributes zeros; (2, 2048,
+# 640): 32 tiles over 11 parts, both groups busy.
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+@pytest.mark.parametrize("B,T,C", [(3, 300, 384), (2, 2048, 640)])
+@pytest.mark.parametrize("residual", [False, True])
+def test_static_tma_kernels(W, B, T, C, residual):
+    x, w, dy = _inputs(B, T, C, W, torch.bfloat16, seed=W + T + C)
+    y, dx, dw = _run(x, w, dy, residual)
+    assert_fwd(y, orc.static_fwd(x, w, residual), torch.bfloat16)
+    rdx, rdw = orc.static_bwd(x, w, dy, residual)
+    assert_grad(dx, rdx, torch.bfloat16, "dx")
+    assert_grad(dw, rdw, torch.bfloat16, "dw")
+
+
+def test_static_tma_kernels_qkv_size():
+    # the benchmark's shape: 96 chunks x 3 parts, y and dx on 4096 sampled
+    # rows, all of dw
+    B, T, C, W = 8, 2048, 6144, 4
+    x, w, dy = _inputs(B, T, C, W, torch.bfloat16, seed=21)
+    y, dx, dw = _run(x, w, dy, True)
+    rows = syn.sample_rows(B, T, W, 4096, seed=5)
+    assert_fwd(rows_of(y, rows), orc.static_fwd(x, w, True, rows=rows), torch.bfloat16)
+    assert_grad(rows_of(dx, rows), orc.static_dx_rows(w, dy, True, T, rows), torch.bfloat16, "dx")
+    _, rdw = orc.static_bwd(x, w, dy, True)
+    assert_grad(dw, rdw, torch.bfloat16, "dw")
+    assert dsc.dsc_device_error() == 0
+
+
 def test_static_dw_is_bitwise_reproducible():
     x, w, dy = _inputs(4, 1024, 1024, 4, torch.bfloat16, seed=2)
     _, _, dw1 = _run(x, w, dy, True)
